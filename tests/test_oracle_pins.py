@@ -1,0 +1,326 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+Every pin below rests on the pages or on mathematics, never on the oracle:
+worked examples printed on the pages (tests/golden/), closed forms, invariants,
+wraparound arithmetic done with Python's unbounded integers, and brute-force
+O(n^2) prefix sums computed from scratch on tiny inputs.  The same pin suite is
+run against a set of deliberately broken scans (a dropped term, a wrong sign, an
+off-by-one shift, a reversed or transposed walk, the wrong operator...) to show
+that a plausible mistake anywhere fails at least one pin.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN_DEF = "merry_definitions_example.txt"
+GOLDEN_KS = "merry_kogge_stone_example.txt"
+GOLDEN_KARY = "merry_kary_brent_kung_example.txt"
+GOLDEN_PACK = "merry_output_format_example.txt"
+
+
+def oracle_scan3(x, op, inclusive, init=None):
+    return oracle.scan3(x, op, inclusive, init)
+
+
+def one_d(scan3, x, op="add", inclusive=True, init=None):
+    return scan3(np.asarray(x).reshape(1, -1, 1), op, inclusive, init).reshape(-1)
+
+
+# ---------------------------------------------------------------- the pins --
+
+def pin_golden_definitions(scan3, golden):
+    g = golden(GOLDEN_DEF)
+    for dt in (np.int32, np.int64, np.float32, np.float64):
+        x = np.array(g["input"], dtype=dt)
+        assert list(one_d(scan3, x)) == g["inclusive"]
+        assert list(one_d(scan3, x, inclusive=False)) == g["exclusive"]
+
+
+def pin_golden_kogge_stone(scan3, golden):
+    g = golden(GOLDEN_KS)
+    x = np.array(g["input"], dtype=np.int32)
+    assert list(one_d(scan3, x)) == g["inclusive"]
+
+
+def pin_golden_kary(scan3, golden):
+    g = golden(GOLDEN_KARY)
+    x = np.array(g["input"], dtype=np.int32)
+    inc = [int(v) for v in one_d(scan3, x)]
+    exc = [int(v) for v in one_d(scan3, x, inclusive=False)]
+    b = g["block_size"][0]
+    assert inc == g["inclusive"]
+    assert inc[-1] == g["total"][0]
+    # Block sums and the exclusive block bases of the 4-ary down-sweep.
+    ends = [inc[k * b + b - 1] for k in range(len(x) // b)]
+    assert [ends[0]] + [ends[k] - ends[k - 1] for k in range(1, len(ends))] == g["block_sums"]
+    assert [exc[k * b] for k in range(len(x) // b)] == g["block_bases"]
+
+
+def pin_all_ones(scan3, golden=None):
+    for dt, n in ((np.int32, 100_003), (np.int64, 4097), (np.float32, 70_000), (np.float64, 5000)):
+        x = np.ones(n, dtype=dt)
+        assert np.array_equal(one_d(scan3, x), np.arange(1, n + 1))
+        assert np.array_equal(one_d(scan3, x, inclusive=False), np.arange(0, n))
+
+
+def pin_last_is_reduction(scan3, golden=None):
+    r = np.random.default_rng(101)
+    xi = r.integers(-2**31, 2**31, 5000, dtype=np.int64).astype(np.int32)
+    total = sum(int(v) for v in xi) % 2**32
+    total = total - 2**32 if total >= 2**31 else total
+    assert int(one_d(scan3, xi)[-1]) == total
+    xf = r.standard_normal(20_000)
+    bound = 2 * len(xf) * np.finfo(np.float64).eps * np.abs(xf).sum()
+    assert abs(float(one_d(scan3, xf)[-1]) - math.fsum(xf)) <= bound
+    xm = r.standard_normal(3000).astype(np.float32)
+    assert float(one_d(scan3, xm, "max")[-1]) == float(xm.max())
+    assert float(one_d(scan3, xm, "min")[-1]) == float(xm.min())
+
+
+def pin_max_min_monotone(scan3, golden=None):
+    up = np.arange(-500, 500, dtype=np.int32)
+    down = up[::-1].copy()
+    assert np.array_equal(one_d(scan3, up, "max"), up)
+    assert np.array_equal(one_d(scan3, down, "max"), np.full(down.size, down[0]))
+    assert np.array_equal(one_d(scan3, down, "min"), down)
+    assert np.array_equal(one_d(scan3, up, "min"), np.full(up.size, up[0]))
+    upf = np.linspace(-3, 3, 777).astype(np.float32)
+    assert np.array_equal(one_d(scan3, upf, "max"), upf.astype(np.float64))
+
+
+def pin_exclusive_relations(scan3, golden=None):
+    r = np.random.default_rng(7)
+    x = r.integers(-1000, 1000, 4000).astype(np.int32)
+    s = one_d(scan3, x).astype(np.int64)
+    e = one_d(scan3, x, inclusive=False).astype(np.int64)
+    assert np.array_equal(e, s - x)           # e = s - x for (invertible) add
+    assert e[0] == 0 and np.array_equal(e[1:], s[:-1])
+    xf = r.standard_normal(3000).astype(np.float32)
+    sm = one_d(scan3, xf, "max")
+    em = one_d(scan3, xf, "max", inclusive=False, init=xf[0])
+    assert em[0] == xf[0] and np.array_equal(em[1:], sm[:-1])   # e_i = s_{i-1}
+    e5 = one_d(scan3, x, inclusive=False, init=5).astype(np.int64)
+    assert np.array_equal(e5, e + 5)          # init folds in on the left
+
+
+def pin_wraparound(scan3, golden=None):
+    x = np.array([2**31 - 1, 1, 2**31 - 1, 2**31 - 1, -5, 7], dtype=np.int32)
+    acc, want = 0, []
+    for v in x:
+        acc = (acc + int(v)) % 2**32
+        want.append(acc - 2**32 if acc >= 2**31 else acc)
+    assert [int(v) for v in one_d(scan3, x)] == want
+    xu = np.array([2**32 - 1, 2, 2**32 - 3], dtype=np.uint32)
+    acc, wantu = 0, []
+    for v in xu:
+        acc = (acc + int(v)) % 2**32
+        wantu.append(acc)
+    assert [int(v) for v in one_d(scan3, xu)] == wantu
+
+
+def _brute(x, op, inclusive, init):
+    """Every prefix recomputed from scratch: O(n^2)."""
+    n = len(x)
+    out = []
+    for i in range(n):
+        terms = list(x[: i + 1]) if inclusive else list(x[:i])
+        if not inclusive and init is not None:
+            terms = [init] + terms
+        if op == "add":
+            out.append(math.fsum(terms) if isinstance(terms[0] if terms else 0.0, float) else sum(terms))
+        elif op == "max":
+            out.append(max(terms))
+        else:
+            out.append(min(terms))
+    return out
+
+
+def pin_bruteforce(scan3, golden=None):
+    r = np.random.default_rng(2024)
+    for n in (1, 2, 31, 33, 257):
+        xi = r.integers(-50, 50, n).astype(np.int64)
+        for op in ("add", "max", "min"):
+            got = [int(v) for v in one_d(scan3, xi, op)]
+            assert got == _brute([int(v) for v in xi], op, True, None)
+            got = [int(v) for v in one_d(scan3, xi, op, False, init=3)]
+            assert got == _brute([int(v) for v in xi], op, False, 3)
+        xf = r.standard_normal(n)
+        tol = 2 * n * np.finfo(np.float64).eps * np.cumsum(np.abs(xf))
+        got = one_d(scan3, xf, "add")
+        want = np.array(_brute([float(v) for v in xf], "add", True, None))
+        assert np.all(np.abs(got - want) <= tol)
+        for op in ("max", "min"):
+            assert list(one_d(scan3, xf, op)) == _brute([float(v) for v in xf], op, True, None)
+
+
+def pin_axes_and_lanes(scan3, golden=None):
+    """A (B, R, C) scan is B*C independent 1-D scans along R."""
+    r = np.random.default_rng(5)
+    B, R, C = 3, 41, 5
+    x = r.integers(-9, 9, (B, R, C)).astype(np.int32)
+    got = scan3(x, "add", True)
+    for b in range(B):
+        for c in range(C):
+            want = _brute([int(v) for v in x[b, :, c]], "add", True, None)
+            assert [int(v) for v in got[b, :, c]] == want
+    got = scan3(x, "add", False, [1, 2, 3, 4, 5])
+    for c in range(C):
+        want = _brute([int(v) for v in x[0, :, c]], "add", False, c + 1)
+        assert [int(v) for v in got[0, :, c]] == want
+
+
+PINS = [pin_golden_definitions, pin_golden_kogge_stone, pin_golden_kary, pin_all_ones,
+        pin_last_is_reduction, pin_max_min_monotone, pin_exclusive_relations,
+        pin_wraparound, pin_bruteforce, pin_axes_and_lanes]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_oracle_scan_pins(pin, golden):
+    pin(oracle_scan3, golden)
+
+
+def test_exclusive_max_needs_init():
+    with pytest.raises(oracle.NoIdentity):
+        oracle.scan(np.arange(5, dtype=np.float32), "max", inclusive=False)
+    with pytest.raises(oracle.NoIdentity):
+        oracle.scan(np.arange(5, dtype=np.int32), "min", inclusive=False)
+
+
+def test_oracle_wrapper_axes(golden):
+    """scan_batched's axis mapping: axis 1 = rows, axis 0 = columns (row-major)."""
+    r = np.random.default_rng(9)
+    m = r.integers(-5, 5, (7, 11)).astype(np.int32)
+    rows = oracle.scan_batched(m, axis=1)
+    cols = oracle.scan_batched(m, axis=0)
+    for i in range(7):
+        assert np.array_equal(rows[i], oracle.scan(m[i]))
+    for j in range(11):
+        assert np.array_equal(cols[:, j], oracle.scan(np.ascontiguousarray(m[:, j])))
+
+
+# ------------------------------------------ the pins catch planted mistakes --
+
+def _numpy_scan3(mistake):
+    """A scan3 built from numpy with one plausible mistake planted in it."""
+    def scan3(x, op, inclusive, init=None):
+        x = np.asarray(x)
+        acc_t = np.float64 if x.dtype.kind == "f" else x.dtype
+        if mistake == "fp32_accumulate" and x.dtype.kind == "f":
+            acc_t = np.float32
+        a = x.astype(acc_t)
+        axis = 2 if mistake == "transposed_axis" else 1
+        if mistake == "reversed":
+            a = np.flip(a, axis=axis)
+        use = op
+        if mistake == "max_is_min":
+            use = {"max": "min", "min": "max"}.get(op, op)
+        if mistake == "drop_first_term":
+            a = a.copy()
+            idx = [slice(None)] * 3
+            idx[axis] = 0
+            if use == "add":
+                a[tuple(idx)] = 0
+        if use == "add":
+            if mistake == "wrong_sign":
+                s = np.cumsum(-a, axis=axis) + 2 * np.take(a, [0], axis=axis)
+            else:
+                s = np.cumsum(a, axis=axis, dtype=acc_t)
+        elif use == "max":
+            s = np.maximum.accumulate(a, axis=axis)
+        else:
+            s = np.minimum.accumulate(a, axis=axis)
+        if mistake == "reversed":
+            s = np.flip(s, axis=axis)
+        if mistake == "off_by_one":
+            inclusive = not inclusive
+        if inclusive:
+            return s
+        first = np.zeros_like(np.take(s, [0], axis=axis))
+        if init is not None and mistake != "init_ignored":
+            first = first + np.asarray(init, dtype=acc_t).reshape(1, 1, -1)
+            if use == "add":
+                s = s + np.asarray(init, dtype=acc_t).reshape(1, 1, -1)
+            elif use == "max":
+                s = np.maximum(s, np.asarray(init, dtype=acc_t).reshape(1, 1, -1))
+            else:
+                s = np.minimum(s, np.asarray(init, dtype=acc_t).reshape(1, 1, -1))
+        shifted = np.concatenate([first, np.delete(s, -1, axis=axis)], axis=axis)
+        return shifted
+    return scan3
+
+
+MISTAKES = ["drop_first_term", "wrong_sign", "off_by_one", "reversed", "transposed_axis",
+            "max_is_min", "init_ignored", "fp32_accumulate"]
+
+
+def test_reference_numpy_scan_passes(golden):
+    """The numpy stand-in without a planted mistake passes every pin."""
+    for pin in PINS:
+        pin(_numpy_scan3("none"), golden)
+
+
+@pytest.mark.parametrize("mistake", MISTAKES)
+def test_pins_catch_planted_mistake(mistake, golden):
+    failures = 0
+    for pin in PINS:
+        try:
+            pin(_numpy_scan3(mistake), golden)
+        except (AssertionError, ValueError, IndexError):
+            failures += 1
+    assert failures >= 1, "no pin caught the planted mistake %r" % mistake
+
+
+# ------------------------------------------------------------- compaction --
+
+def test_compact_invariants_and_bruteforce():
+    r = np.random.default_rng(55)
+    x = r.random(50_001, dtype=np.float32)
+    for pred, p in (("lt", 0.01), ("lt", 0.5), ("lt", 0.99), ("ge", 0.5), ("eq", float(x[17])),
+                    ("ne", float(x[3])), ("le", 0.25), ("gt", 0.75)):
+        idx = oracle.compact(x, pred, p)
+        t = np.float32(p)
+        mask = {"lt": x < t, "le": x <= t, "gt": x > t, "ge": x >= t, "eq": x == t, "ne": x != t}[pred]
+        assert idx.size == int(mask.sum())                     # count = sum of predicate bits
+        assert np.all(np.diff(idx) > 0)                        # stable, strictly ascending
+        assert np.array_equal(idx, np.nonzero(mask)[0])        # brute force
+        assert np.all(mask[idx])
+
+
+def test_compact_special_cases():
+    x = np.linspace(0, 1, 1000, endpoint=False).astype(np.float32)
+    assert oracle.compact(x, "lt", 0.0).size == 0              # selects none
+    assert np.array_equal(oracle.compact(x, "lt", 2.0), np.arange(1000))   # selects all
+    assert oracle.compact(np.zeros(0, np.float32), "lt", 1.0).size == 0
+    nan = np.array([np.nan, 1.0, np.nan], dtype=np.float32)
+    assert list(oracle.compact(nan, "ne", 1.0)) == [0, 2]      # NaN != t holds
+    assert list(oracle.compact(nan, "lt", 5.0)) == [1]         # NaN < t does not
+    xi = np.array([5, -3, 7, 0], dtype=np.int32)
+    assert list(oracle.compact(xi, "gt", 0)) == [0, 2]
+
+
+# ---------------------------------------------------------------- packing --
+
+def test_pack_golden(golden):
+    g = golden(GOLDEN_PACK)
+    offs, recs, total = oracle.pack_by_counts(np.array(g["counts"], dtype=np.int32))
+    assert list(offs) == g["offsets"]
+    assert list(recs) == g["records"]
+    assert total == g["total"][0]
+
+
+def test_pack_invariants():
+    r = np.random.default_rng(6)
+    k = r.poisson(4.0, 20_000).astype(np.int32)
+    offs, recs, total = oracle.pack_by_counts(k)
+    assert total == int(k.astype(np.int64).sum())
+    assert np.array_equal(offs, np.concatenate([[0], np.cumsum(k, dtype=np.int64)[:-1]]))
+    assert np.array_equal(recs, np.repeat(np.arange(k.size, dtype=np.int32), k))
+    # capacity truncates the records but not the total
+    offs2, recs2, total2 = oracle.pack_by_counts(k, capacity=1000)
+    assert total2 == total and np.array_equal(recs2, recs[:1000])
+    # empty input and all-zero counts
+    assert oracle.pack_by_counts(np.zeros(0, np.int32))[2] == 0
+    assert oracle.pack_by_counts(np.zeros(10, np.int32))[2] == 0
