@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Benchmark: device-wide scan and stream compaction on one GB300 (or N replicas).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--headline-only]
+
+One step is one fp32 inclusive scan of n = 1e8 values ~ N(0,1) through the C ABI
+(gb_scan_inclusive: status reset + the single-pass kernel), with the input already
+in HBM.  The step is timed with CUDA events on the launching stream; the kernel alone
+is timed through the library's profile-event hook.  Rank 0 prints ONE JSON line.
+
+Besides the headline, the line carries the other workloads (int32/fp64/max scans,
+compaction, packing, batched and large-element scans, the reduce-then-scan variant)
+under "workloads", each as kernel time, GB/s and fraction of the HBM roofline, L2
+flushed between repetitions.  --impl reference times the CPU oracle instead.
+
+Multi-GPU: the scan does not shard here; N > 1 runs N independent replicas (one per
+rank, no collective on the data path) and reports their aggregate throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fp32 1e8 inclusive scan GB/s (% of HBM peak); compaction Gelem/s"
+HEADLINE = "fp32_1e8"
+N_HEAD = 100_000_000
+BYTES_HEAD = 2 * N_HEAD * 4            # read once, write once (single pass)
+# AcceleratedKernels.jl PR #208, RTX 5080, cumsum F32 1e8: 1388.2 us (context only).
+PAGE_FP32_1E8_US = 1388.2
+PAGE_FP32_1E8_GBS = BYTES_HEAD / (PAGE_FP32_1E8_US * 1e-6) / 1e9
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- helpers ------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s)"
+
+
+def kernel_source_hash() -> str:
+    d = os.path.join(ROOT, "stream_compaction_decoupled_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str):
+    """DRAM bytes per launch recorded by an ncu capture of this exact kernel source.
+
+    The summaries under profiles/ carry 'kernel:', 'source_hash:' and
+    'traffic_bytes_per_launch:' lines; a figure taken on an older source is ignored.
+    """
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    src = kernel_source_hash()
+    for f in sorted(os.listdir(d)):
+        if not f.endswith(".md"):
+            continue
+        txt = open(os.path.join(d, f)).read()
+        k = re.search(r"^kernel:\s*(\S+)", txt, re.M)
+        h = re.search(r"^source_hash:\s*(\S+)", txt, re.M)
+        t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt, re.M)
+        if k and h and t and k.group(1) == kernel and h.group(1) == src:
+            return float(t.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms in the background."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "gbscan_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                    except ValueError:
+                        continue
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "no samples (nvidia-smi unavailable)"}
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if not inside:  # the timed region was shorter than the sampling period
+            inside = [r for r in rows if r[0] >= t0 - 2.0]
+            window = "benchmark load around the timed region (timed region < sampling period)"
+        if not inside:
+            inside, window = rows, "whole run"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[3][i].lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def dist_init():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return 0, 1, 0
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (1 rank: the value itself)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index] if device is not None else None)
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------- GPU workloads -----
+
+class L2Flush:
+    """Writes a buffer of twice the L2 size between repetitions."""
+
+    def __init__(self, device):
+        import torch
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.buf = torch.empty(max(2 * l2, 64 << 20) // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_call(fn, reps: int, flush, stream, kernel_events: bool):
+    """Best and median kernel time (ms) of fn() over reps, L2 flushed before each."""
+    import torch
+    import stream_compaction_decoupled_gb300 as gb
+    ks, steps = [], []
+    for _ in range(reps):
+        if flush:
+            flush()
+        kb, ka = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sb, sa = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if kernel_events:
+            gb.set_profile_events(kb, ka)
+        sb.record(stream)
+        fn()
+        sa.record(stream)
+        gb.set_profile_events(None, None)
+        torch.cuda.synchronize()
+        steps.append(sb.elapsed_time(sa))
+        if kernel_events:
+            ks.append(kb.elapsed_time(ka))
+    k = ks if kernel_events else steps
+    return {"kernel_ms_best": min(k), "kernel_ms_median": float(np.median(k)),
+            "step_ms_median": float(np.median(steps))}
+
+
+def secondary_workloads(device, hbm_peak, reps=10):
+    """Every other workload: kernel time, GB/s, fraction of the HBM roofline."""
+    import torch
+    import stream_compaction_decoupled_gb300 as gb
+    from stream_compaction_decoupled_gb300 import workloads as W
+    stream = torch.cuda.current_stream(device)
+    flush = L2Flush(device)
+    out = {}
+    for w in W.WORKLOADS:
+        if w.name == HEADLINE:
+            continue
+        x = torch.from_numpy(w.make()).to(device)
+        es = x.element_size()
+        if w.kind == "scan":
+            y = torch.empty_like(x)
+            n_el = x.numel()
+            if w.inclusive:
+                fn = lambda: gb.scan_inclusive(x, w.op, lanes=w.lanes, out=y)  # noqa: E731
+            else:
+                fn = lambda: gb.scan_exclusive(x, w.op, lanes=w.lanes, out=y)  # noqa: E731
+            nbytes, units, unit = 2 * n_el * es, n_el // w.lanes, "Gelem/s"
+        elif w.kind == "batched":
+            rows, cols = w.shape
+            xv = x.reshape(rows, cols, w.lanes)
+            y = torch.empty_like(xv)
+            fn = lambda: gb.scan_batched(xv, axis=w.axis, op=w.op, lanes=w.lanes, out=y)  # noqa: E731
+            nbytes, units, unit = 2 * x.numel() * es, rows * cols, "Gelem/s"
+        elif w.kind == "compact":
+            idx = torch.empty(x.numel(), dtype=torch.int32, device=device)
+            cnt = torch.empty(1, dtype=torch.int32, device=device)
+            p = w.extra["p"]
+            fn = lambda: gb.compact(x, "lt", p, out_idx=idx, out_count=cnt)  # noqa: E731
+            fn()
+            torch.cuda.synchronize()
+            m = int(cnt.item())
+            nbytes, units, unit = 4 * x.numel() + 4 * m + 4, x.numel(), "Gelem/s"
+        else:  # pack
+            total = int(x.sum().item())
+            recs = torch.empty(total, dtype=torch.int32, device=device)
+            tot = torch.empty(1, dtype=torch.int32, device=device)
+            fn = lambda: gb.pack_by_counts(x, total, offsets=True, out_records=recs, out_total=tot)  # noqa: E731
+            nbytes, units, unit = 4 * x.numel() * 2 + 4 * total, x.numel(), "Gelem/s"
+        for _ in range(3):
+            fn()
+        t = time_call(fn, reps, flush, stream, kernel_events=True)
+        ms = t["kernel_ms_best"]
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[w.name] = {"kernel_us_best": round(ms * 1e3, 2), "kernel_us_median": round(t["kernel_ms_median"] * 1e3, 2),
+                       "step_us_median": round(t["step_ms_median"] * 1e3, 2),
+                       "GB_s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4),
+                       "throughput": round(units / (ms * 1e-3) / 1e9, 3), "throughput_unit": unit,
+                       "algorithmic_bytes": int(nbytes), "l2": "flushed between repetitions"}
+        del x
+    # The reduce-then-scan comparison variant on the headline workload.
+    xh = torch.from_numpy(W.BY_NAME[HEADLINE].make()).to(device)
+    yh = torch.empty_like(xh)
+    fn = lambda: gb.scan_reduce_then_scan(xh, out=yh)  # noqa: E731
+    for _ in range(3):
+        fn()
+    t = time_call(fn, reps, None, stream, kernel_events=False)
+    ms = t["kernel_ms_best"]
+    out["fp32_1e8_reduce_then_scan"] = {
+        "step_us_best": round(ms * 1e3, 2), "step_us_median": round(t["kernel_ms_median"] * 1e3, 2),
+        "GB_s": round(BYTES_HEAD / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(BYTES_HEAD / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+        "algorithmic_bytes": BYTES_HEAD, "note": "three launches; 2n-byte model, so 3n traffic shows as a lower GB/s"}
+    return out
+
+
+# ---------------------------------------------------------------- CPU oracle ---
+
+def cpu_oracle_leg(x_full: np.ndarray, steps: int, budget_s: float):
+    """The oracle timed on the host: `steps` inclusive scans of a leading slice of the
+    headline input, its length chosen so that all steps take about budget_s."""
+    import oracle
+    cal = x_full[:1_000_000]
+    t0 = time.perf_counter()
+    oracle.scan(cal)
+    per_elem = max((time.perf_counter() - t0) / cal.size, 1e-10)
+    n = int(min(x_full.size, max(1_000_000, budget_s / max(steps, 1) / per_elem)))
+    x = x_full[:n]
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.scan(x)
+        times.append(time.perf_counter() - t0)
+    return n, times
+
+
+def reference_arm(args, rank):
+    """--impl reference: the CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    from stream_compaction_decoupled_gb300 import workloads as W
+    n, times = cpu_oracle_leg(W.BY_NAME[HEADLINE].make(), args.warmup + args.steps, budget_s=60.0)
+    times = times[args.warmup:] or times
+    t = float(np.mean(times))
+    gbs = 2 * n * 4 / t / 1e9
+    sample = ("fp32 inclusive scan of the first %d of the 1e8 N(0,1) seed-2 values, one thread, "
+              "%d timed steps after %d warm-up" % (n, args.steps, args.warmup))
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 in, f64 accumulate",
+            "data": "synthetic", "config": {"workload": "fp32_1e8 inclusive scan (sample, see cpu_baseline)"},
+            "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm ------
+
+def our_arm(args, rank, world, local_rank):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import stream_compaction_decoupled_gb300 as gb
+    from stream_compaction_decoupled_gb300 import workloads as W
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    hbm_peak, peak_src = peaks()
+    stream = torch.cuda.current_stream(device)
+
+    x_host = W.BY_NAME[HEADLINE].make()
+    x = torch.from_numpy(x_host).to(device)
+    y = torch.empty_like(x)
+    temp = torch.empty(gb.temp_storage_bytes(gb.KIND_SCAN, gb.F32, 1, N_HEAD), dtype=torch.uint8, device=device)
+    step = lambda: gb.scan_inclusive(x, out=y, temp=temp)  # noqa: E731
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(device.index if world == 1 else int(os.environ.get("LOCAL_RANK", "0")))
+    if rank == 0:
+        sampler.start()
+    k_before = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k_after = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        gb.set_profile_events(k_before[i], k_after[i])
+        step()
+    gb.set_profile_events(None, None)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(device)
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total_max = max_over_ranks(ms_total, device)
+    kernel_ms = float(np.mean([b.elapsed_time(a) for b, a in zip(k_before, k_after)]))
+    if gb.device_error() != gb.OK:
+        raise RuntimeError("device-side error during the timed region")
+
+    # End to end through the same C ABI: pinned host input -> device -> scan -> host.
+    xh = torch.from_numpy(x_host).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    e2e_steps = max(3, min(args.steps, 30))
+    for _ in range(2):
+        x.copy_(xh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(xh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, device)
+    barrier(device)
+
+    extra = None
+    if rank == 0 and not args.headline_only and world == 1:
+        extra = secondary_workloads(device, hbm_peak)
+    if rank == 0:
+        sampler.stop()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_s, times = cpu_oracle_leg(x_host, 3, budget_s=30.0)
+        t = min(times)
+        cpu = {"value": round(2 * n_s * 4 / t / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "fp32 inclusive scan of %d of the headline's values (fp64 accumulation), best of 3, "
+                         "one host thread" % n_s}
+
+    if rank != 0:
+        return
+    ms_per_step = ms_total_max / args.steps
+    value = world * BYTES_HEAD / (ms_per_step * 1e-3) / 1e9
+    achieved = BYTES_HEAD / (kernel_ms * 1e-3) / 1e9
+    traffic = traffic_from_profiles("scan_rows_kernel<float,add>")
+    clocks = sampler.summary(t_wall0, t_wall1)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": round(value / world / PAGE_FP32_1E8_GBS, 3),
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "fp32_1e8: inclusive add scan of n=1e8 fp32 ~N(0,1), seed 2, 1-D contiguous",
+                   "n": N_HEAD, "l2": "inputs larger than L2 (400 MB in + 400 MB out vs 129 MB L2), no flush",
+                   "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "step": "gb_scan_inclusive = status reset (cudaMemsetAsync, 195 KB) + one single-pass kernel"},
+        "frac_of_hbm_peak": round(value / world / hbm_peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     "kernel": "scan_rows_kernel<float,add>", "kernel_us_mean": round(kernel_ms * 1e3, 2),
+                     "algorithmic_bytes_per_launch": BYTES_HEAD, "peak_source": peak_src},
+        "e2e": {"value": round(world * BYTES_HEAD / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": N_HEAD * 4, "d2h_bytes_per_step": N_HEAD * 4, "steps": e2e_steps,
+                "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": args.steps, "memsets_per_step": 1,
+        "clocks": clocks,
+        "compaction_headline": None,
+        "cpu_baseline": cpu,
+        "page_context": {"rtx5080_fp32_1e8_us": PAGE_FP32_1E8_US, "rtx5080_fp32_1e8_GB_s": round(PAGE_FP32_1E8_GBS, 1)},
+    }
+    if extra:
+        line["workloads"] = extra
+        c = extra.get("compact_p0.5")
+        if c:
+            line["compaction_headline"] = {"workload": "compact_p0.5 (fp32 1e7, x<0.5)",
+                                           "value": c["throughput"], "unit": "Gelem/s"}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    rank, world, local_rank = dist_init()
+    if args.impl == "reference":
+        reference_arm(args, rank)
+    else:
+        our_arm(args, rank, world, local_rank)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+/*
+ * gbscan.h -- device-wide prefix sums and stream compaction for the NVIDIA GB300
+ * (sm_103a), as a plain C ABI.
+ *
+ * The operations are those of three pages on the subject:
+ *   [HB]  The CUDA Handbook, ch. 13 "Scan", section 13.3 "CUDA implementations"
+ *         (13.3.1 warp and block scans; 13.3.3 reduce-then-scan, Listings 13-10..
+ *         13-12, Figure 13-10; 13.3.4 single-pass decoupled look-back, Figure
+ *         13-11, Listings 13-13..13-15; 13.3.5 items per thread, Listing 13-16).
+ *   [PS]  B. Merry, "Prefix sums on GPUs", GPGPU2 2014: slides "Exclusive Prefix
+ *         Sum", "Inclusive Prefix Sum", "Output Format", "Solution", "Other
+ *         Applications", "Fixed Block Count", "Prefix-Summing a Block".
+ *   [AK]  AcceleratedKernels.jl PR #208, "Fit the scans' tiles in local memory for
+ *         large element types": tiles sized per element type; ScanPrefixes,
+ *         SliceScan along `dims`, findall.
+ *
+ * Conventions shared by every call:
+ *   - All data pointers (in, out, out_idx, counts, offsets, records, out_count,
+ *     out_total, temp) are DEVICE pointers owned by the caller.  `init` and
+ *     `threshold` are HOST pointers to one element, read during the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every call is asynchronous on that stream; nothing synchronises
+ *     unless stated.
+ *   - An "element" is `lanes` consecutive values of `dtype` (lanes = 1 for plain
+ *     arrays; 24 fp32 lanes for a 96-byte struct; 17 fp64 lanes for a dual number
+ *     with 16 partials).  Operators act lane-wise.
+ *   - `temp` may be NULL: the library then draws scratch from the stream-ordered
+ *     allocator (cudaMallocAsync / cudaFreeAsync on `stream`), as [HB] 13.3.4's
+ *     host function does (Listing 13-15).  Otherwise it must point to at least
+ *     gb_temp_storage_bytes(...) bytes, 256-byte aligned, not used concurrently
+ *     by another call.  The library resets the parts it needs on every call.
+ *   - In-place scans (in == out) are allowed.  out_idx / out_records must not
+ *     overlap the inputs.
+ *   - n = 0 (or rows*cols = 0) is a no-op that returns GB_OK; compaction and
+ *     packing still write a count of 0.
+ *   - Return value: GB_OK or one of the GB_ERR_* codes below.  Argument errors
+ *     are reported before anything is enqueued.  Errors found on the device
+ *     (a look-back that waited too long, a packing capacity exceeded, a negative
+ *     count) are sticky per device and are read with gb_device_error().
+ */
+#ifndef GBSCAN_H
+#define GBSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+enum gb_dtype { GB_I32 = 0, GB_U32 = 1, GB_I64 = 2, GB_U64 = 3, GB_F32 = 4, GB_F64 = 5 };
+
+/* Associative operators ([PS] "Exclusive Prefix Sum": an operator (+) with an
+ * identity I; "Other Applications": max for visibility).  ADD wraps modulo 2^32 /
+ * 2^64 for integers.  MAX / MIN on floats follow fmax / fmin (a NaN operand is
+ * ignored).  MAX and MIN are treated as operators WITHOUT a neutral element
+ * ([AK]): inclusive scans need none, exclusive scans need `init`. */
+enum gb_op { GB_ADD = 0, GB_MAX = 1, GB_MIN = 2 };
+
+/* Compaction predicates: element x is selected when  x <op> threshold. */
+enum gb_pred { GB_LT = 0, GB_LE = 1, GB_GT = 2, GB_GE = 3, GB_EQ = 4, GB_NE = 5 };
+
+/* Kinds for gb_temp_storage_bytes. */
+enum gb_kind {
+  GB_KIND_SCAN = 0,          /* gb_scan_inclusive / gb_scan_exclusive: rows = n      */
+  GB_KIND_BATCHED_AXIS1 = 1, /* gb_scan_batched axis 1: rows x cols                   */
+  GB_KIND_BATCHED_AXIS0 = 2, /* gb_scan_batched axis 0: rows x cols                   */
+  GB_KIND_COMPACT = 3,       /* gb_compact: rows = n                                  */
+  GB_KIND_PACK = 4,          /* gb_pack_by_counts: rows = n                           */
+  GB_KIND_REDUCE_THEN_SCAN = 5 /* gb_scan_reduce_then_scan: rows = n                  */
+};
+
+/* Status codes. */
+enum gb_status {
+  GB_OK = 0,
+  GB_ERR_INVALID = 1,     /* null pointer, negative size, lanes < 1, bad axis/enum   */
+  GB_ERR_UNSUPPORTED = 2, /* dtype / op / lanes combination not provided              */
+  GB_ERR_TEMP = 3,        /* temp_bytes smaller than gb_temp_storage_bytes           */
+  GB_ERR_NO_IDENTITY = 4, /* exclusive MAX / MIN without init                         */
+  GB_ERR_RANGE = 5,       /* too large for int32 indices, or packing over capacity   */
+  GB_ERR_CUDA = 6,        /* a CUDA runtime call failed: see gb_last_cuda_error()     */
+  GB_ERR_TIMEOUT = 7      /* (device) a look-back or copy wait hit its time limit     */
+};
+
+/*
+ * Inclusive scan  s_i = a_0 (+) ... (+) a_i  of n elements ([PS] "Inclusive Prefix
+ * Sum"), computed in one pass by decoupled look-back ([HB] 13.3.4-13.3.5).
+ *   dtype, lanes, op  element type, lanes per element (1..4096), operator
+ *   in, out           n*lanes values each, contiguous, row-major (element-major)
+ *   temp, temp_bytes  scratch (see conventions); kind GB_KIND_SCAN
+ * Errors: GB_ERR_INVALID, GB_ERR_UNSUPPORTED, GB_ERR_TEMP, GB_ERR_CUDA.
+ */
+int gb_scan_inclusive(int dtype, int lanes, int op, const void* in, void* out, int64_t n,
+                      void* temp, size_t temp_bytes, void* stream);
+
+/*
+ * Exclusive scan  e_i = init (+) a_0 (+) ... (+) a_{i-1}  ([PS] "Exclusive Prefix
+ * Sum"; the caller's init takes the place of the identity I and is folded in on
+ * the left of every output).  `init` is a host pointer to one element (lanes
+ * values) or NULL: NULL means 0 for GB_ADD and is refused for MAX / MIN with
+ * GB_ERR_NO_IDENTITY.  The exclusive value is the prefix of the predecessors (a
+ * shift), not inclusive minus x ([HB] 13.3.1 derives it by subtraction, which
+ * holds for add only).
+ */
+int gb_scan_exclusive(int dtype, int lanes, int op, const void* in, void* out, int64_t n,
+                      const void* init, void* temp, size_t temp_bytes, void* stream);
+
+/*
+ * Batched scans of a row-major (rows, cols) matrix of elements ([AK] SliceScan
+ * along `dims`).
+ *   axis = 1  scan along each row (contiguous; every row is independent)
+ *   axis = 0  scan down each column (stride cols*lanes)
+ *   inclusive 1 for inclusive, 0 for exclusive (init as in gb_scan_exclusive,
+ *             applied to every row / column)
+ * temp kind: GB_KIND_BATCHED_AXIS1 or GB_KIND_BATCHED_AXIS0.
+ */
+int gb_scan_batched(int dtype, int lanes, int op, int inclusive, const void* in, void* out,
+                    int64_t rows, int64_t cols, int axis, const void* init,
+                    void* temp, size_t temp_bytes, void* stream);
+
+/*
+ * Stream compaction ([PS] "Other Applications": compaction; "Solution": count,
+ * scan, emit): writes to out_idx, in ascending order, the int32 index of every
+ * element x_i (lanes = 1) with  x_i <pred> *threshold, the comparison made in
+ * `dtype`, and the number selected to *out_count (device).  One pass: per-tile
+ * counts, decoupled look-back over the counts, staged scatter.  Stable ([PS]
+ * "Atomics": order must be preserved).  out_idx must hold up to n entries.
+ * Errors: GB_ERR_RANGE if n > INT32_MAX.  temp kind: GB_KIND_COMPACT.
+ */
+int gb_compact(int dtype, const void* in, int64_t n, int pred, const void* threshold,
+               int32_t* out_idx, int32_t* out_count, void* temp, size_t temp_bytes,
+               void* stream);
+
+/*
+ * Variable-length packing ([PS] "Output Format" and "Solution"): object i emits
+ * counts[i] records holding the value i; its run starts at the exclusive prefix
+ * sum of the counts, and the runs are packed contiguously into out_records.
+ *   offsets       NULL, or n int32 entries that receive the start of each run
+ *   out_capacity  entries available in out_records; records past it are dropped
+ *   out_total     device int32: the total record count (sum of counts)
+ * Device errors (gb_device_error): GB_ERR_RANGE when the total exceeds
+ * out_capacity or INT32_MAX; GB_ERR_INVALID when a count is negative (it is then
+ * treated as 0).  temp kind: GB_KIND_PACK.
+ */
+int gb_pack_by_counts(const int32_t* counts, int64_t n, int32_t* offsets,
+                      int32_t* out_records, int64_t out_capacity, int32_t* out_total,
+                      void* temp, size_t temp_bytes, void* stream);
+
+/*
+ * The reduce-then-scan comparison variant ([HB] 13.3.3, Listings 13-10..13-12;
+ * [PS] "Fixed Block Count"): a fixed number C of blocks (a multiple of the SM
+ * count) each reduce a contiguous subarray, one block scans the C partials, then
+ * each block scans its subarray starting from its base.  Three launches, 3n
+ * element transfers instead of 2n.  lanes = 1.  Same results and errors as the
+ * single-pass scans; temp kind GB_KIND_REDUCE_THEN_SCAN.
+ */
+int gb_scan_reduce_then_scan(int dtype, int op, int inclusive, const void* in, void* out,
+                             int64_t n, const void* init, void* temp, size_t temp_bytes,
+                             void* stream);
+
+/*
+ * Scratch bytes a call needs for the given kind and sizes (rows = n for the 1-D
+ * kinds; cols ignored there).  Returns 0 for an invalid combination.
+ */
+size_t gb_temp_storage_bytes(int kind, int dtype, int lanes, int64_t rows, int64_t cols);
+
+/*
+ * Synchronise `stream`, then return and clear the sticky device-side error of the
+ * current device: GB_OK, GB_ERR_TIMEOUT, GB_ERR_RANGE or GB_ERR_INVALID (the
+ * first kind seen since the last read), or GB_ERR_CUDA if the sync failed.
+ */
+int gb_device_error(void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* gb_status_string(int status);
+
+/* The cudaError_t value behind the last GB_ERR_CUDA returned on this thread. */
+int gb_last_cuda_error(void);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int gb_version(void);
+
+/*
+ * Observability hook: when both are non-NULL cudaEvent_t handles, the next calls
+ * on this host thread record `before` and `after` on their stream immediately
+ * around their main kernel launch (the single-pass kernel, or the last of the
+ * reduce-then-scan launches), so a caller can time that kernel alone.  Pass
+ * NULL, NULL to turn it off.
+ */
+void gb_set_profile_events(void* before, void* after);
+
+/*
+ * Time limit, in nanoseconds of the GPU's global timer, of every wait inside the
+ * kernels (a look-back waiting on a predecessor, a tile waiting for its copy).  A
+ * wait that runs out records GB_ERR_TIMEOUT (see gb_device_error), publishes what
+ * it has so that later tiles do not wait as well, and the kernel returns normally.
+ * 0 restores the default of one second.  Process-wide.
+ */
+void gb_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Fault injection for tests: the tile with this index (in claim order) of the
+ * next single-pass launches never publishes its status, so its successors' waits
+ * run out.  -1 (the default) turns it off.  Process-wide.
+ */
+void gb_set_stalled_tile(int64_t tile);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBSCAN_H */

@@ -1,0 +1,373 @@
+// api.cu -- the C ABI declared in include/gbscan.h: argument checks, scratch
+// (temp) handling, element-type dispatch and the sticky device error word.
+// Every check that can fail does so before anything is enqueued.
+#include <atomic>
+#include <mutex>
+#include <type_traits>
+#include <vector>
+
+#include "common.cuh"
+#include "gbscan.h"
+#include "launch.h"
+
+// Sticky device-side error bits (look-back / copy timeouts, packing overflow,
+// negative counts), one word per device, set with atomicOr by the kernels.
+__device__ unsigned g_gbscan_device_error;
+
+namespace {
+
+using gbs::LaunchCtx;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxLanes = 4096;
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // 1 s
+
+std::mutex g_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+std::atomic<unsigned long long> g_wait_ns{0};
+std::atomic<long long> g_stalled_tile{-1};
+thread_local int t_last_cuda = 0;
+thread_local cudaEvent_t t_ev_before = nullptr;
+thread_local cudaEvent_t t_ev_after = nullptr;
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda = (int)e;
+  return GB_ERR_CUDA;
+}
+
+// Per-device set-up (once): the address of the error word and the SM count.
+int make_ctx(void* stream, LaunchCtx& ctx) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return GB_ERR_UNSUPPORTED;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_gbscan_device_error);
+      if (e != cudaSuccess) return cuda_fail(e);
+      int sms = 0;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(e);
+      g_num_sms[dev] = sms;
+      g_err_ptr[dev] = (unsigned*)p;
+    }
+    ctx.err = g_err_ptr[dev];
+    ctx.num_sms = g_num_sms[dev];
+  }
+  ctx.stream = (cudaStream_t)stream;
+  const unsigned long long w = g_wait_ns.load();
+  ctx.wait_ns = w ? w : kDefaultWaitNs;
+  ctx.stalled_tile = g_stalled_tile.load();
+  ctx.ev_before = t_ev_before;
+  ctx.ev_after = t_ev_after;
+  return GB_OK;
+}
+
+// Caller-supplied scratch, or stream-ordered scratch freed when the call ends.
+struct Temp {
+  void* p = nullptr;
+  bool owned = false;
+  cudaStream_t s = nullptr;
+  ~Temp() {
+    if (owned && p) cudaFreeAsync(p, s);
+  }
+};
+
+int get_temp(void* temp, size_t temp_bytes, size_t need, cudaStream_t s, Temp& t) {
+  t.s = s;
+  if (temp) {
+    if (temp_bytes < need) return GB_ERR_TEMP;
+    if ((uintptr_t)temp % 256) return GB_ERR_INVALID;
+    t.p = temp;
+    return GB_OK;
+  }
+  cudaError_t e = cudaMallocAsync(&t.p, need, s);
+  if (e != cudaSuccess) {
+    t.p = nullptr;
+    return cuda_fail(e);
+  }
+  t.owned = true;
+  return GB_OK;
+}
+
+size_t dtype_size(int dtype) {
+  switch (dtype) {
+    case GB_I32: case GB_U32: case GB_F32: return 4;
+    case GB_I64: case GB_U64: case GB_F64: return 8;
+    default: return 0;
+  }
+}
+
+bool valid_op(int op) { return op == GB_ADD || op == GB_MAX || op == GB_MIN; }
+
+// Calls f.template operator()<T>() with T the C++ type of `dtype`.
+template <class F> auto with_type(int dtype, F&& f) {
+  switch (dtype) {
+    case GB_I32: return f((int32_t*)nullptr);
+    case GB_U32: return f((uint32_t*)nullptr);
+    case GB_I64: return f((int64_t*)nullptr);
+    case GB_U64: return f((uint64_t*)nullptr);
+    case GB_F32: return f((float*)nullptr);
+    default: return f((double*)nullptr);
+  }
+}
+
+// Tiles are claimed with a 32-bit counter and indexed with grid.x.
+constexpr size_t kMaxTiles = 0x7fffffffull;
+
+size_t scan_temp(int dtype, long long B, long long R, long long C) {
+  return with_type(dtype, [&](auto* tp) -> size_t {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::scan_temp_bytes<T>(B, R, C);
+  });
+}
+
+bool scan_fits(int dtype, long long B, long long R, long long C) {
+  // Conservative bound on the tile count of either kernel (tiles hold >= 64 positions
+  // of a lane strip, or >= 2048 positions of a row).
+  const size_t es = dtype_size(dtype);
+  const long long strips = C <= 1 ? 1 : (C + 31) / 32;
+  const long long per = C <= 1 ? (es == 4 ? 4096 : 2048) : 8;
+  const long double tiles = (long double)B * strips * ((R + per - 1) / per);
+  return tiles < (long double)kMaxTiles;
+}
+
+// Shared body of every scan entry point: (B, R, C) layout, init lanes.
+int run_scan(int dtype, int op, int inclusive, const void* in, void* out, long long B, long long R,
+             long long C, const void* init, int lanes, void* temp, size_t temp_bytes, void* stream) {
+  if (!dtype_size(dtype) || !valid_op(op)) return GB_ERR_INVALID;
+  if (lanes < 1 || lanes > kMaxLanes || B < 0 || R < 0 || C < 0) return GB_ERR_INVALID;
+  if (!inclusive && !init && op != GB_ADD) return GB_ERR_NO_IDENTITY;
+  if (B == 0 || R == 0 || C == 0) return GB_OK;
+  if (!in || !out) return GB_ERR_INVALID;
+  if ((long double)B * R * C > 9.0e18L) return GB_ERR_RANGE;
+  if (!scan_fits(dtype, B, R, C)) return GB_ERR_RANGE;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  Temp t;
+  rc = get_temp(temp, temp_bytes, scan_temp(dtype, B, R, C), ctx.stream, t);
+  if (rc) return rc;
+  std::vector<unsigned char> zeros;
+  if (!inclusive && !init) {  // add without init: start from 0
+    zeros.assign((size_t)lanes * dtype_size(dtype), 0);
+    init = zeros.data();
+  }
+  gbs::ScanJob job;
+  job.op = op;
+  job.inclusive = inclusive ? 1 : 0;
+  job.in = in;
+  job.out = out;
+  job.B = B;
+  job.R = R;
+  job.C = C;
+  job.init_host = init;
+  job.init_lanes = lanes;
+  job.temp = t.p;
+  const cudaError_t e = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::launch_scan<T>(job, ctx);
+  });
+  if (e != cudaSuccess) return cuda_fail(e);
+  return GB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gb_scan_inclusive(int dtype, int lanes, int op, const void* in, void* out, int64_t n, void* temp,
+                      size_t temp_bytes, void* stream) {
+  if (n < 0) return GB_ERR_INVALID;
+  return run_scan(dtype, op, 1, in, out, 1, n, lanes, nullptr, lanes, temp, temp_bytes, stream);
+}
+
+int gb_scan_exclusive(int dtype, int lanes, int op, const void* in, void* out, int64_t n, const void* init,
+                      void* temp, size_t temp_bytes, void* stream) {
+  if (n < 0) return GB_ERR_INVALID;
+  return run_scan(dtype, op, 0, in, out, 1, n, lanes, init, lanes, temp, temp_bytes, stream);
+}
+
+int gb_scan_batched(int dtype, int lanes, int op, int inclusive, const void* in, void* out, int64_t rows,
+                    int64_t cols, int axis, const void* init, void* temp, size_t temp_bytes, void* stream) {
+  if (rows < 0 || cols < 0 || lanes < 1 || lanes > kMaxLanes) return GB_ERR_INVALID;
+  if (axis == 1) return run_scan(dtype, op, inclusive, in, out, rows, cols, lanes, init, lanes, temp, temp_bytes, stream);
+  if (axis == 0) {
+    if (cols != 0 && (long double)cols * lanes > 9.0e18L) return GB_ERR_RANGE;
+    return run_scan(dtype, op, inclusive, in, out, 1, rows, (long long)cols * lanes, init, lanes, temp, temp_bytes,
+                    stream);
+  }
+  return GB_ERR_INVALID;
+}
+
+int gb_compact(int dtype, const void* in, int64_t n, int pred, const void* threshold, int32_t* out_idx,
+               int32_t* out_count, void* temp, size_t temp_bytes, void* stream) {
+  if (!dtype_size(dtype) || pred < GB_LT || pred > GB_NE || n < 0) return GB_ERR_INVALID;
+  if (!out_count || !threshold) return GB_ERR_INVALID;
+  if (n > 0x7fffffffll) return GB_ERR_RANGE;
+  if (n > 0 && (!in || !out_idx)) return GB_ERR_INVALID;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  if (n == 0) {
+    cudaError_t e = cudaMemsetAsync(out_count, 0, sizeof(int32_t), ctx.stream);
+    return e == cudaSuccess ? GB_OK : cuda_fail(e);
+  }
+  const size_t need = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::compact_temp_bytes<T>(n);
+  });
+  Temp t;
+  rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
+  if (rc) return rc;
+  gbs::CompactJob job;
+  job.in = in;
+  job.n = n;
+  job.pred = pred;
+  job.threshold_host = threshold;
+  job.out_idx = out_idx;
+  job.out_count = out_count;
+  job.temp = t.p;
+  const cudaError_t e = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::launch_compact<T>(job, ctx);
+  });
+  return e == cudaSuccess ? GB_OK : cuda_fail(e);
+}
+
+int gb_pack_by_counts(const int32_t* counts, int64_t n, int32_t* offsets, int32_t* out_records,
+                      int64_t out_capacity, int32_t* out_total, void* temp, size_t temp_bytes, void* stream) {
+  if (n < 0 || out_capacity < 0 || !out_total) return GB_ERR_INVALID;
+  if (n > 0x7fffffffll) return GB_ERR_RANGE;
+  if (n > 0 && !counts) return GB_ERR_INVALID;
+  if (out_capacity > 0 && !out_records) return GB_ERR_INVALID;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  if (n == 0) {
+    cudaError_t e = cudaMemsetAsync(out_total, 0, sizeof(int32_t), ctx.stream);
+    return e == cudaSuccess ? GB_OK : cuda_fail(e);
+  }
+  Temp t;
+  rc = get_temp(temp, temp_bytes, gbs::pack_temp_bytes(n), ctx.stream, t);
+  if (rc) return rc;
+  gbs::PackJob job;
+  job.counts = counts;
+  job.n = n;
+  job.offsets = offsets;
+  job.records = out_records;
+  job.capacity = out_capacity;
+  job.out_total = out_total;
+  job.temp = t.p;
+  const cudaError_t e = gbs::launch_pack(job, ctx);
+  return e == cudaSuccess ? GB_OK : cuda_fail(e);
+}
+
+int gb_scan_reduce_then_scan(int dtype, int op, int inclusive, const void* in, void* out, int64_t n,
+                             const void* init, void* temp, size_t temp_bytes, void* stream) {
+  if (!dtype_size(dtype) || !valid_op(op) || n < 0) return GB_ERR_INVALID;
+  if (!inclusive && !init && op != GB_ADD) return GB_ERR_NO_IDENTITY;
+  if (n == 0) return GB_OK;
+  if (!in || !out) return GB_ERR_INVALID;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  const size_t need = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::rts_temp_bytes<T>(n, ctx.num_sms);
+  });
+  Temp t;
+  rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
+  if (rc) return rc;
+  unsigned long long zero = 0;
+  gbs::RtsJob job;
+  job.op = op;
+  job.inclusive = inclusive ? 1 : 0;
+  job.in = in;
+  job.out = out;
+  job.n = n;
+  job.init_host = init ? init : &zero;
+  job.temp = t.p;
+  const cudaError_t e = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::launch_rts<T>(job, ctx);
+  });
+  return e == cudaSuccess ? GB_OK : cuda_fail(e);
+}
+
+size_t gb_temp_storage_bytes(int kind, int dtype, int lanes, int64_t rows, int64_t cols) {
+  if (!dtype_size(dtype) || lanes < 1 || lanes > kMaxLanes || rows < 0 || cols < 0) return 0;
+  switch (kind) {
+    case GB_KIND_SCAN:
+      return scan_temp(dtype, 1, rows, lanes);
+    case GB_KIND_BATCHED_AXIS1:
+      return scan_temp(dtype, rows, cols, lanes);
+    case GB_KIND_BATCHED_AXIS0:
+      return scan_temp(dtype, 1, rows, (long long)cols * lanes);
+    case GB_KIND_COMPACT:
+      return with_type(dtype, [&](auto* tp) {
+        using T = std::remove_pointer_t<decltype(tp)>;
+        return gbs::compact_temp_bytes<T>(rows);
+      });
+    case GB_KIND_PACK:
+      return gbs::pack_temp_bytes(rows);
+    case GB_KIND_REDUCE_THEN_SCAN:
+      return with_type(dtype, [&](auto* tp) {
+        using T = std::remove_pointer_t<decltype(tp)>;
+        return gbs::rts_temp_bytes<T>(rows, 0);
+      });
+    default:
+      return 0;
+  }
+}
+
+int gb_device_error(void* stream) {
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(ctx.stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned bits = 0;
+  e = cudaMemcpy(&bits, ctx.err, sizeof(bits), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (bits) {
+    e = cudaMemset(ctx.err, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (bits & gbs::ERRBIT_TIMEOUT) return GB_ERR_TIMEOUT;
+  if (bits & gbs::ERRBIT_RANGE) return GB_ERR_RANGE;
+  if (bits & gbs::ERRBIT_INVALID) return GB_ERR_INVALID;
+  return GB_OK;
+}
+
+const char* gb_status_string(int status) {
+  switch (status) {
+    case GB_OK: return "GB_OK";
+    case GB_ERR_INVALID: return "GB_ERR_INVALID: invalid argument";
+    case GB_ERR_UNSUPPORTED: return "GB_ERR_UNSUPPORTED: unsupported type, operator or size";
+    case GB_ERR_TEMP: return "GB_ERR_TEMP: temporary storage too small";
+    case GB_ERR_NO_IDENTITY: return "GB_ERR_NO_IDENTITY: exclusive max/min needs an initial value";
+    case GB_ERR_RANGE: return "GB_ERR_RANGE: size or output capacity out of range";
+    case GB_ERR_CUDA: return "GB_ERR_CUDA: a CUDA runtime call failed";
+    case GB_ERR_TIMEOUT: return "GB_ERR_TIMEOUT: a device-side wait ran out of time";
+    default: return "unknown gbscan status";
+  }
+}
+
+int gb_last_cuda_error(void) { return t_last_cuda; }
+
+int gb_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+void gb_set_profile_events(void* before, void* after) {
+  t_ev_before = (cudaEvent_t)before;
+  t_ev_after = (cudaEvent_t)after;
+}
+
+void gb_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
+
+void gb_set_stalled_tile(int64_t tile) { g_stalled_tile.store(tile); }
+
+}  // extern "C"

@@ -1,0 +1,42 @@
+// scan.cuh -- dispatch of a scan along the middle axis of a row-major (B, R, C)
+// array: C == 1 (contiguous rows) goes to the row kernel, C > 1 (lanes / columns)
+// to the lane kernel.
+#pragma once
+
+#include "scan_lanes.cuh"
+#include "scan_rows.cuh"
+
+namespace gbs {
+
+template <class T> size_t scan_temp_bytes(long long B, long long R, long long C) {
+  if (C == 1) return kHeaderBytes + rows_status_bytes<T>(rows_tiles<T>(B, R));
+  return lanes_temp_bytes<T>(B, R, C);
+}
+
+template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& ctx) {
+  if (job.C == 1) {
+    switch (job.op) {
+      case OP_ADD: return launch_rows_op<T, OP_ADD>(job, ctx);
+      case OP_MAX: return launch_rows_op<T, OP_MAX>(job, ctx);
+      default: return launch_rows_op<T, OP_MIN>(job, ctx);
+    }
+  }
+  switch (job.op) {
+    case OP_ADD: return launch_lanes_op<T, OP_ADD>(job, ctx);
+    case OP_MAX: return launch_lanes_op<T, OP_MAX>(job, ctx);
+    default: return launch_lanes_op<T, OP_MIN>(job, ctx);
+  }
+}
+
+}  // namespace gbs
+
+// Explicit instantiation of every launcher for one element type.
+#define GBS_INSTANTIATE(T)                                                                   \
+  namespace gbs {                                                                            \
+  template size_t scan_temp_bytes<T>(long long, long long, long long);                      \
+  template cudaError_t launch_scan<T>(const ScanJob&, const LaunchCtx&);                    \
+  template size_t compact_temp_bytes<T>(long long);                                         \
+  template cudaError_t launch_compact<T>(const CompactJob&, const LaunchCtx&);              \
+  template size_t rts_temp_bytes<T>(long long, int);                                        \
+  template cudaError_t launch_rts<T>(const RtsJob&, const LaunchCtx&);                      \
+  }

@@ -1,0 +1,218 @@
+// scan_rows.cuh -- single-pass decoupled look-back scan of contiguous rows: a 1-D
+// scan is one row; a batched scan along axis 1 of a row-major matrix is one row
+// per matrix row.  Tiles never cross a row, and a row's tile 0 publishes its
+// inclusive prefix at once, so the look-back stops at the start of the row.
+//
+// Per tile (one CTA, claimed in order from an atomic counter; The CUDA Handbook,
+// 13.3.4-13.3.5, Listings 13-14 and 13-16):
+//   1. claim the tile index; one thread issues a bulk (TMA) copy of the whole
+//      tile into shared memory, completing on an mbarrier (a ragged or unaligned
+//      tile is loaded with plain coalesced loads instead);
+//   2. pass 1: per-(round, lane) serial combine of a 16-byte vector, warp scans
+//      of the lane totals, per-warp totals;
+//   3. block scan of the warp totals (warp 0) -> tile aggregate;
+//   4. warp 0 publishes A (or P for a row's first tile) and looks back;
+//      publishes P;
+//   5. pass 2 rewrites the tile in shared memory with the final values;
+//   6. one thread bulk-copies the tile back to global memory.
+#pragma once
+
+#include "launch.h"
+#include "tile.cuh"
+
+namespace gbs {
+
+template <class T> struct RowsArgs {
+  const T* in;
+  T* out;
+  long long R;              // elements per row
+  unsigned tiles_per_row;   // ceil(R / TILE)
+  unsigned num_tiles;       // rows * tiles_per_row
+  unsigned* counter;        // tile-claim counter, 0 on entry
+  unsigned* err;            // sticky device error word
+  T init;                   // exclusive scans: folded in on the left of every row
+  int inclusive;
+  int bulk_ok;              // in, out and every row start are 16-byte aligned
+  unsigned long long wait_ns;
+  long long stalled_tile;
+};
+
+template <class T> struct RowsGeom {
+  static constexpr int NT = 256;
+  static constexpr int NW = NT / 32;
+  static constexpr int ROUNDS = 4;
+  static constexpr int VEC = 16 / (int)sizeof(T);
+  static constexpr int TILE = NW * ROUNDS * 32 * VEC;  // 4096 x 4 B, 2048 x 8 B: 16 KB
+};
+
+template <class T, int OP, class S>
+__global__ void __launch_bounds__(RowsGeom<T>::NT) scan_rows_kernel(RowsArgs<T> a, S st) {
+  using G = RowsGeom<T>;
+  constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, TILE = G::TILE;
+  __shared__ __align__(128) T s_tile[TILE];
+  __shared__ __align__(8) unsigned long long s_bar;
+  __shared__ unsigned s_t;
+  __shared__ T s_warp[NW];
+  __shared__ T s_prefix;
+  __shared__ int s_has_prefix;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (tid == 0) {
+    const unsigned t = atomicAdd(a.counter, 1u);
+    s_t = t;
+    const unsigned row = t / a.tiles_per_row, tt = t - row * a.tiles_per_row;
+    const long long off = (long long)tt * TILE;
+    if (a.bulk_ok && a.R - off >= TILE) {
+      mbar_init(&s_bar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&s_bar, TILE * sizeof(T));
+      bulk_g2s(s_tile, a.in + (long long)row * a.R + off, TILE * sizeof(T), &s_bar);
+    }
+  }
+  __syncthreads();
+  const unsigned t = s_t;
+  const unsigned row = t / a.tiles_per_row, tt = t - row * a.tiles_per_row;
+  const long long off = (long long)tt * TILE;
+  const long long start = (long long)row * a.R + off;
+  const int len = a.R - off >= TILE ? TILE : (int)(a.R - off);
+  const bool bulk = a.bulk_ok && len == TILE;
+
+  bool failed = false;
+  if (bulk) {
+    failed = !mbar_wait(&s_bar, 0, a.wait_ns);
+  } else {
+    const T* src = a.in + start;
+    for (int k = tid; k < TILE; k += NT) s_tile[k] = k < len ? src[k] : T{};
+  }
+  if (__syncthreads_or(failed)) {
+    // The copy never landed: record it, let successors go on, write nothing.
+    if (tid == 0) {
+      atomicOr(a.err, ERRBIT_TIMEOUT);
+      mbar_wait(&s_bar, 0, a.wait_ns);  // give the copy in flight one more bounded wait
+      if ((long long)t != a.stalled_tile) {
+        S(st).publish((long long)row * a.tiles_per_row + tt, FLAG_P, T{});
+      }
+    }
+    return;
+  }
+
+  // Pass 1.
+  uint4* run = reinterpret_cast<uint4*>(s_tile) + warp * ROUNDS * 32;
+  T pre[ROUNDS];
+  const T wtot = tile_reduce_pass<T, OP, ROUNDS>(run, lane, pre);
+  if (lane == 0) s_warp[warp] = wtot;
+  __syncthreads();
+
+  // Block scan of warp totals, then the look-back, both by warp 0.
+  if (warp == 0) {
+    const T agg = block_scan_warp_totals<T, OP, NW>(s_warp, lane);
+    const long long first = (long long)row * a.tiles_per_row;
+    const bool stalled = (long long)t == a.stalled_tile;
+    if (tt == 0) {
+      if (lane == 0) {
+        if (!stalled) st.publish(first, FLAG_P, agg);
+        s_has_prefix = 0;
+      }
+    } else {
+      if (lane == 0 && !stalled) st.publish(first + tt, FLAG_A, agg);
+      bool timed_out;
+      const T pfx = lookback_warp<T, OP>(st, first, tt, a.wait_ns, timed_out);
+      if (lane == 0) {
+        if (!stalled) st.publish(first + tt, FLAG_P, Op<T, OP>::f(pfx, agg));
+        s_prefix = pfx;
+        s_has_prefix = 1;
+        if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+      }
+    }
+  }
+  __syncthreads();
+
+  // Pass 2: base = tile prefix (+) warps before this one (+ init on the left).
+  bool has_base = s_has_prefix != 0;
+  T base = s_prefix;
+  if (warp > 0) {
+    const T wp = s_warp[warp - 1];
+    base = has_base ? Op<T, OP>::f(base, wp) : wp;
+    has_base = true;
+  }
+  if (!a.inclusive) {
+    base = has_base ? Op<T, OP>::f(a.init, base) : a.init;
+    has_base = true;
+  }
+  tile_apply_pass<T, OP, ROUNDS>(run, lane, pre, base, has_base, a.inclusive != 0);
+
+  if (bulk) {
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_s2g(a.out + start, s_tile, TILE * sizeof(T));
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  } else {
+    __syncthreads();
+    T* dst = a.out + start;
+    for (int k = tid; k < len; k += NT) dst[k] = s_tile[k];
+  }
+}
+
+// Status area of the row kernel, right after the header.
+template <class T> size_t rows_status_bytes(unsigned num_tiles) {
+  if (sizeof(T) == 4) return round_up((size_t)num_tiles * 8, 256);
+  return round_up((size_t)num_tiles * 4, 256) + 2 * round_up((size_t)num_tiles * sizeof(T), 256);
+}
+// Bytes the per-call reset has to clear (counter + flags).
+template <class T> size_t rows_reset_bytes(unsigned num_tiles) {
+  if (sizeof(T) == 4) return kHeaderBytes + round_up((size_t)num_tiles * 8, 256);
+  return kHeaderBytes + round_up((size_t)num_tiles * 4, 256);
+}
+
+template <class T> unsigned rows_tiles(long long B, long long R) {
+  const long long tpr = (R + RowsGeom<T>::TILE - 1) / RowsGeom<T>::TILE;
+  return (unsigned)(B * tpr);
+}
+
+template <class T> typename StatusFor<T>::type rows_status(void* temp, unsigned num_tiles) {
+  char* base = (char*)temp + kHeaderBytes;
+  typename StatusFor<T>::type st;
+  if constexpr (sizeof(T) == 4) {
+    st.w = (unsigned long long*)base;
+  } else {
+    st.flag = (unsigned*)base;
+    base += round_up((size_t)num_tiles * 4, 256);
+    st.agg = (T*)base;
+    base += round_up((size_t)num_tiles * sizeof(T), 256);
+    st.pfx = (T*)base;
+  }
+  return st;
+}
+
+template <class T, int OP>
+cudaError_t launch_rows_op(const ScanJob& job, const LaunchCtx& ctx) {
+  using G = RowsGeom<T>;
+  RowsArgs<T> a;
+  a.in = (const T*)job.in;
+  a.out = (T*)job.out;
+  a.R = job.R;
+  a.tiles_per_row = (unsigned)((job.R + G::TILE - 1) / G::TILE);
+  a.num_tiles = rows_tiles<T>(job.B, job.R);
+  a.counter = (unsigned*)job.temp;
+  a.err = ctx.err;
+  a.init = T{};
+  if (!job.inclusive && job.init_host) memcpy(&a.init, job.init_host, sizeof(T));
+  a.inclusive = job.inclusive;
+  a.bulk_ok = ((uintptr_t)job.in % 16 == 0) && ((uintptr_t)job.out % 16 == 0) &&
+              (job.B == 1 || (job.R * (long long)sizeof(T)) % 16 == 0);
+  a.wait_ns = ctx.wait_ns;
+  a.stalled_tile = ctx.stalled_tile;
+  auto st = rows_status<T>(job.temp, a.num_tiles);
+  cudaError_t e = cudaMemsetAsync(job.temp, 0, rows_reset_bytes<T>(a.num_tiles), ctx.stream);
+  if (e != cudaSuccess) return e;
+  profile_before(ctx);
+  scan_rows_kernel<T, OP, decltype(st)><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
+  profile_after(ctx);
+  return cudaGetLastError();
+}
+
+}  // namespace gbs

@@ -1,0 +1,276 @@
+// tile.cuh -- the pieces of a single-pass tile scan shared by every kernel:
+// tile-status descriptors, the decoupled look-back, and the two passes over a tile
+// held in shared memory.
+//
+// A tile of TILE = NW warps x ROUNDS x 32 lanes x VEC elements lives in shared
+// memory in its natural order.  Warp w owns the contiguous run
+// [w*ROUNDS*32*VEC, (w+1)*ROUNDS*32*VEC); in round j lane l owns the 16-byte vector
+// at j*32 + l of that run.  Reading the tile this way is a conflict-free 128-bit
+// shared-memory access, and every element is read by exactly one thread.
+//
+// Pass 1 (reduce) gives each (round, lane) the combination of all warp elements
+// before it and each warp its total; the block scan of the warp totals gives each
+// warp its offset and the tile its aggregate; the look-back gives the tile its
+// exclusive prefix; pass 2 (apply) rewrites the tile in place with the scanned
+// values.  Each element is read twice and written once in shared memory; in global
+// memory it is read once and written once (The CUDA Handbook, 13.3.4: 2N traffic).
+#pragma once
+
+#include "common.cuh"
+
+namespace gbs {
+
+// ---- tile-status descriptors -------------------------------------------------------
+
+// 4-byte values: one 64-bit word per tile holding (flag << 32) | value bits,
+// written and read whole, so a reader that sees the flag sees the matching value
+// and no fence is needed between them (The CUDA Handbook, 13.3.4: the packed
+// descriptor).  The value is bit-cast, not value-cast, so floats survive.
+template <class T> struct PackedStatus {
+  unsigned long long* w;
+  __device__ __forceinline__ void publish(long long i, unsigned flag, T v) const {
+    st_relaxed_u64(w + i, ((unsigned long long)flag << 32) | to_u32(v));
+  }
+  __device__ __forceinline__ unsigned poll(long long i, T& v) const {
+    unsigned long long x = ld_relaxed_u64(w + i);
+    v = from_u32<T>((unsigned)x);
+    return (unsigned)(x >> 32);
+  }
+  __device__ __forceinline__ T fetch(long long, unsigned, T polled) const { return polled; }
+};
+
+// 8-byte (or wider) values: the two-word descriptor with an explicit fence that
+// the same section names for 64-bit types.  The value goes to a slot of its own
+// (aggregate and inclusive prefix have separate slots, so a reader that saw A can
+// never pick up the later P value), then the flag is stored with release
+// semantics; a reader loads the flag with acquire semantics before the value.
+template <class T> struct SplitStatus {
+  unsigned* flag;
+  T* agg;
+  T* pfx;
+  __device__ __forceinline__ void publish(long long i, unsigned f, T v) const {
+    st_relaxed(f == FLAG_A ? agg + i : pfx + i, v);
+    st_release_u32(flag + i, f);
+  }
+  __device__ __forceinline__ unsigned poll(long long i, T&) const { return ld_acquire_u32(flag + i); }
+  __device__ __forceinline__ T fetch(long long i, unsigned f, T) const {
+    return ld_relaxed(f == FLAG_A ? agg + i : pfx + i);
+  }
+};
+
+template <class T> struct StatusFor {
+  using type = typename std::conditional<sizeof(T) == 4, PackedStatus<T>, SplitStatus<T>>::type;
+};
+
+// ---- decoupled look-back -------------------------------------------------------------
+
+// Warp-cooperative look-back (The CUDA Handbook, 13.3.4, Figure 13-11): lane k
+// inspects predecessor frontier-k, so the warp reads the 32 nearest predecessors
+// at once; it re-reads while a tile it still needs is X; a ballot finds the
+// nearest P; the values from the frontier back to that P are combined in tile
+// order (earlier tiles on the left); with no P in the window, all 32 aggregates
+// are combined and the warp steps back 32 tiles.  A tile only needs its window up
+// to the nearest P to be non-X, not the whole window.
+//
+// `first` is the status index of tile 0 of this row (whose status is always P),
+// `tt` >= 1 the tile's index within the row.  Called by all 32 lanes of one warp;
+// returns the tile's exclusive prefix in every lane.  Every wait is bounded by
+// wait_ns of global time; on expiry *timed_out is set and whatever was read is
+// returned.
+template <class T, int OP, class S>
+__device__ __forceinline__ T lookback_warp(const S& st, long long first, long long tt,
+                                           unsigned long long wait_ns, bool& timed_out) {
+  const int lane = threadIdx.x & 31;
+  long long frontier = tt - 1;
+  T acc{};
+  bool have = false;
+  timed_out = false;
+  for (;;) {
+    const long long p = frontier - lane;
+    unsigned f = FLAG_P;
+    T v{};
+    int spins = 0;
+    unsigned long long t0 = 0;
+    for (;;) {
+      f = (p >= 0) ? st.poll(first + p, v) : FLAG_P;  // before the row: stops the walk
+      const unsigned pm = __ballot_sync(0xffffffffu, f == FLAG_P);
+      const unsigned xm = __ballot_sync(0xffffffffu, f == FLAG_X);
+      const unsigned need = pm ? (pm ^ (pm - 1u)) : 0xffffffffu;  // lanes 0..nearest P
+      if ((xm & need) == 0) break;
+      // The time-out decision is taken by the whole warp at once, so no lane leaves
+      // the loop while others still poll (the ballots above need every lane).
+      if (spins == 0) t0 = __shfl_sync(0xffffffffu, globaltimer(), 0);
+      const bool late = spins > 0 && __shfl_sync(0xffffffffu, globaltimer(), 0) - t0 > wait_ns;
+      if (late) {
+        timed_out = true;
+        break;
+      }
+      backoff(spins++);
+    }
+    const unsigned pm = __ballot_sync(0xffffffffu, f == FLAG_P);
+    const int nearest = pm ? __ffs(pm) - 1 : 32;
+    const int m = nearest < 32 ? nearest : 31;
+    if (lane <= m && p >= 0) v = st.fetch(first + p, f, v);
+    // Ordered combination of lanes 0..m (lane k = tile frontier-k).
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      T o = __shfl_down_sync(0xffffffffu, v, off);
+      if (lane + off <= m) v = Op<T, OP>::f(o, v);
+    }
+    v = __shfl_sync(0xffffffffu, v, 0);
+    acc = have ? Op<T, OP>::f(v, acc) : v;
+    have = true;
+    timed_out = __any_sync(0xffffffffu, timed_out);
+    if (nearest < 32 || timed_out) break;
+    frontier -= 32;
+  }
+  return acc;
+}
+
+// Per-lane look-back for lane-vector tiles: one thread walks back along one lane
+// (column), reading D predecessors at a time; same protocol as lookback_warp.
+// Status of (tile i, lane c) is at index i*CT + c.  `first` is the tile index of
+// the chain's tile 0.
+template <class T, int OP, int D, class S>
+__device__ __forceinline__ T lookback_lane(const S& st, long long first, long long tt, int c, int CT,
+                                           unsigned long long wait_ns, bool& timed_out) {
+  long long f = tt - 1;
+  T acc{};
+  bool have = false;
+  timed_out = false;
+  for (;;) {
+    unsigned fl[D];
+    T v[D];
+    int spins = 0;
+    unsigned long long t0 = 0;
+    for (;;) {
+#pragma unroll
+      for (int k = 0; k < D; ++k) {
+        const long long p = f - k;
+        v[k] = T{};
+        fl[k] = p >= 0 ? st.poll((first + p) * CT + c, v[k]) : FLAG_P;
+      }
+      bool ready = true, seen_p = false;
+#pragma unroll
+      for (int k = 0; k < D; ++k) {
+        if (!seen_p && fl[k] == FLAG_X) ready = false;
+        if (fl[k] == FLAG_P) seen_p = true;
+      }
+      if (ready) break;
+      if (spins == 0) {
+        t0 = globaltimer();
+      } else if (globaltimer() - t0 > wait_ns) {
+        timed_out = true;
+        break;
+      }
+      backoff(spins++);
+    }
+    int m = D - 1;
+    bool found = false;
+#pragma unroll
+    for (int k = D - 1; k >= 0; --k)
+      if (fl[k] == FLAG_P) {
+        m = k;
+        found = true;
+      }
+    T w{};
+    bool hw = false;
+#pragma unroll
+    for (int k = D - 1; k >= 0; --k) {
+      const long long p = f - k;
+      if (k <= m && p >= 0) {
+        T val = st.fetch((first + p) * CT + c, fl[k], v[k]);
+        w = hw ? Op<T, OP>::f(w, val) : val;
+        hw = true;
+      }
+    }
+    if (hw) {
+      acc = have ? Op<T, OP>::f(w, acc) : w;
+      have = true;
+    }
+    if (found || timed_out) break;
+    f -= D;
+  }
+  return acc;
+}
+
+// ---- the two passes over a tile in shared memory ------------------------------------
+
+// Pass 1 over warp `warp`'s run: for each round j, pre[j] receives the combination
+// of all of the warp's elements before lane `lane`'s vector (undefined for round 0,
+// lane 0, which has none).  Returns the warp total (in every lane).
+template <class T, int OP, int ROUNDS>
+__device__ __forceinline__ T tile_reduce_pass(const uint4* run, int lane, T (&pre)[ROUNDS]) {
+  constexpr int VEC = Vec<T>::N;
+  T carry{};
+#pragma unroll
+  for (int j = 0; j < ROUNDS; ++j) {
+    Vec<T> x = ld_vec<T>(run + j * 32 + lane);
+    T t = x.v[0];
+#pragma unroll
+    for (int e = 1; e < VEC; ++e) t = Op<T, OP>::f(t, x.v[e]);
+    const T wi = warp_inclusive<T, OP>(t, lane);
+    const T we = __shfl_up_sync(0xffffffffu, wi, 1);
+    const T rt = __shfl_sync(0xffffffffu, wi, 31);
+    if (j == 0) {
+      pre[0] = we;
+      carry = rt;
+    } else {
+      pre[j] = lane == 0 ? carry : Op<T, OP>::f(carry, we);
+      carry = Op<T, OP>::f(carry, rt);
+    }
+  }
+  return carry;
+}
+
+// Pass 2: rewrite the warp's run in place with scanned values.  `base` (valid when
+// has_base) is everything before the warp's run, already combined with the tile
+// prefix and, for an exclusive scan, the initial value.
+template <class T, int OP, int ROUNDS>
+__device__ __forceinline__ void tile_apply_pass(uint4* run, int lane, const T (&pre)[ROUNDS], T base,
+                                                bool has_base, bool inclusive) {
+  constexpr int VEC = Vec<T>::N;
+#pragma unroll
+  for (int j = 0; j < ROUNDS; ++j) {
+    Vec<T> x = ld_vec<T>(run + j * 32 + lane);
+    T r;
+    bool h;
+    if (j > 0 || lane > 0) {
+      r = has_base ? Op<T, OP>::f(base, pre[j]) : pre[j];
+      h = true;
+    } else {
+      r = base;
+      h = has_base;
+    }
+    Vec<T> y;
+    if (inclusive) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        r = h ? Op<T, OP>::f(r, x.v[e]) : x.v[e];
+        h = true;
+        y.v[e] = r;
+      }
+    } else {  // exclusive: base always holds (the initial value at least)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        y.v[e] = r;
+        r = Op<T, OP>::f(r, x.v[e]);
+      }
+    }
+    st_vec<T>(run + j * 32 + lane, y);
+  }
+}
+
+// Block scan of the NW warp totals by warp 0 (The CUDA Handbook, 13.3.1, Listing
+// 13-5, with one shared slot per warp as in AcceleratedKernels.jl PR #208): on
+// return s_warp[w] holds the inclusive total of warps 0..w; returns the tile
+// aggregate in every lane of warp 0.
+template <class T, int OP, int NW>
+__device__ __forceinline__ T block_scan_warp_totals(T* s_warp, int lane) {
+  T w = s_warp[lane < NW ? lane : NW - 1];
+  w = warp_inclusive<T, OP>(w, lane);
+  if (lane < NW) s_warp[lane] = w;
+  return __shfl_sync(0xffffffffu, w, NW - 1);
+}
+
+}  // namespace gbs

@@ -1,0 +1,54 @@
+"""Comparison helpers for the GPU parity tests (GPU result vs the CPU oracle).
+
+Bars:
+  - integers, max/min, compaction indices, packing: bit-exact (max/min on floats:
+    exact value equality, since they never round);
+  - float add: |gpu - oracle_fp64| <= 1e-5 * (prefix sum of |x|) + 1e-6, element
+    by element and lane by lane, the prefix sum of |x| taken along the scanned axis.
+"""
+import numpy as np
+
+import oracle
+
+REL, ABS = 1e-5, 1e-6
+
+
+def abs_prefix(x3: np.ndarray) -> np.ndarray:
+    """Prefix sums of |x| along axis 1 of a (B, R, C) array, in fp64."""
+    return np.cumsum(np.abs(x3.astype(np.float64)), axis=1)
+
+
+def assert_scan_matches(got: np.ndarray, x3: np.ndarray, op: str, inclusive: bool, init=None,
+                        what: str = ""):
+    """got and x3 are (B, R, C) arrays; the oracle scans x3 along axis 1."""
+    want = oracle.scan3(x3, op, inclusive, init)
+    got = got.reshape(x3.shape)
+    if x3.dtype.kind in "iu" or op != "add":
+        if x3.dtype.kind == "f":
+            ok = got.astype(np.float64) == want
+        else:
+            ok = got == want
+        if not ok.all():
+            bad = np.argwhere(~ok)[:5]
+            raise AssertionError("%s: %d mismatches, first at %s: got %s want %s" % (
+                what, int((~ok).sum()), bad[0].tolist(), got[tuple(bad[0])], want[tuple(bad[0])]))
+        return
+    bound = REL * abs_prefix(x3) + ABS
+    if not inclusive:
+        # the exclusive value at i covers elements < i (plus init)
+        shifted = np.zeros_like(bound)
+        shifted[:, 1:, :] = bound[:, :-1, :]
+        bound = shifted + ABS
+        if init is not None:
+            bound = bound + REL * np.abs(np.asarray(init, dtype=np.float64)).reshape(1, 1, -1)
+    err = np.abs(got.astype(np.float64) - want)
+    ok = err <= bound
+    if not ok.all():
+        bad = np.argwhere(~ok)[:5]
+        b0 = tuple(bad[0])
+        raise AssertionError("%s: %d elements out of tolerance, first at %s: got %r want %r (bound %g)" % (
+            what, int((~ok).sum()), list(b0), float(got[b0]), float(want[b0]), float(bound[b0])))
+
+
+def as3(x: np.ndarray, B: int, R: int, C: int) -> np.ndarray:
+    return np.ascontiguousarray(x).reshape(B, R, C)

@@ -1,0 +1,135 @@
+"""GPU parity: stream compaction and packing by counts against the CPU oracle
+(bit-exact: indices, order, counts, offsets, records)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import stream_compaction_decoupled_gb300 as gb
+from stream_compaction_decoupled_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _cuda():
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+    gb.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def check_compact(x, pred, thr, what=""):
+    idx, cnt = gb.compact(dev(x), pred, thr)
+    want = oracle.compact(x, pred, thr)
+    c = int(cnt.item())
+    assert c == want.size, "%s: count %d, oracle %d" % (what, c, want.size)
+    got = idx[:c].cpu().numpy().astype(np.int64)
+    assert np.array_equal(got, want), "%s: indices differ" % what
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64, np.int32, np.int64])
+@pytest.mark.parametrize("n", [1, 2, 33, 2047, 2048, 2049, 4095, 4096, 4097, 3 * 4096 + 77, 100_003])
+@pytest.mark.parametrize("pred", ["lt", "le", "gt", "ge", "eq", "ne"])
+def test_compact_small(dt, n, pred):
+    if np.dtype(dt).kind == "f":
+        x = workloads.uniform01(n, dt, n + 1)
+        x[::7] = x[0]  # repeated values for eq / ne
+        thr = x[0] if pred in ("eq", "ne") else 0.5
+    else:
+        x = workloads.small_ints(n, n + 1, -10, 10, dtype=dt)
+        thr = 0
+    check_compact(x, pred, thr, "%s n=%d %s" % (np.dtype(dt).name, n, pred))
+
+
+def test_compact_none_all_and_empty():
+    x = workloads.uniform01(3 * 4096 + 5, np.float32, 3)
+    check_compact(x, "lt", 0.0, "none")
+    check_compact(x, "lt", 2.0, "all")
+    idx, cnt = gb.compact(torch.empty(0, dtype=torch.float32, device="cuda"), "lt", 1.0)
+    assert int(cnt.item()) == 0
+
+
+def test_compact_unaligned():
+    x = workloads.uniform01(5 * 4096 + 3, np.float32, 8)
+    xd = dev(x)[1:]
+    idx, cnt = gb.compact(xd, "lt", 0.3)
+    want = oracle.compact(x[1:], "lt", 0.3)
+    c = int(cnt.item())
+    assert c == want.size and np.array_equal(idx[:c].cpu().numpy(), want)
+
+
+def test_compact_nan():
+    x = workloads.uniform01(10_000, np.float32, 4)
+    x[::13] = np.nan
+    for pred in ("lt", "ne", "ge"):
+        check_compact(x, pred, 0.5, "nan " + pred)
+
+
+@pytest.mark.parametrize("p", [0.01, 0.5, 0.99])
+def test_compact_full_size(p):
+    w = workloads.BY_NAME["compact_p%s" % p]
+    x = w.make()
+    check_compact(x, "lt", p, w.name)
+    assert gb.device_error() == gb.OK
+
+
+# ---- packing -----------------------------------------------------------------------
+
+def check_pack(k, what="", capacity=None):
+    total = int(k.astype(np.int64).sum())
+    cap = total if capacity is None else capacity
+    offs, recs, tot = gb.pack_by_counts(dev(k), cap)
+    w_offs, w_recs, w_total = oracle.pack_by_counts(k, capacity=cap)
+    assert int(tot.item()) == w_total, what
+    assert np.array_equal(offs.cpu().numpy()[: k.size].astype(np.int64), w_offs), what + " offsets"
+    assert np.array_equal(recs.cpu().numpy()[:cap], w_recs[:cap]), what + " records"
+
+
+def test_pack_golden(golden):
+    g = golden("merry_output_format_example.txt")
+    k = np.array(g["counts"], dtype=np.int32)
+    offs, recs, tot = gb.pack_by_counts(dev(k), 8)
+    assert list(offs.cpu().numpy()) == g["offsets"]
+    assert list(recs.cpu().numpy()) == g["records"]
+    assert int(tot.item()) == g["total"][0]
+
+
+@pytest.mark.parametrize("n", [1, 5, 4095, 4096, 4097, 3 * 4096 + 77, 200_001])
+def test_pack_small(n):
+    k = workloads.poisson_counts(n, 4.0, n)
+    check_pack(k, "poisson n=%d" % n)
+    z = np.zeros(n, dtype=np.int32)
+    z[::97] = 300  # long runs, most objects empty
+    check_pack(z, "sparse n=%d" % n)
+
+
+def test_pack_full_size():
+    w = workloads.BY_NAME["pack_poisson4_1e6"]
+    check_pack(w.make(), w.name)
+    assert gb.device_error() == gb.OK
+
+
+def test_pack_capacity_and_negative_counts():
+    k = workloads.poisson_counts(10_000, 4.0, 3)
+    total = int(k.sum())
+    offs, recs, tot = gb.pack_by_counts(dev(k), total // 2)
+    assert int(tot.item()) == total
+    _, w_recs, _ = oracle.pack_by_counts(k, capacity=total // 2)
+    assert np.array_equal(recs.cpu().numpy(), w_recs)
+    assert gb.device_error() == gb.ERR_RANGE          # over capacity is reported
+    assert gb.device_error() == gb.OK                 # and cleared once read
+    kn = k.copy()
+    kn[17] = -3
+    ref = kn.copy()
+    ref[17] = 0                                       # a negative count counts as zero
+    offs, recs, tot = gb.pack_by_counts(dev(kn), total)
+    assert gb.device_error() == gb.ERR_INVALID
+    w_offs, w_recs, w_total = oracle.pack_by_counts(ref, capacity=total)
+    assert int(tot.item()) == w_total
+    assert np.array_equal(offs.cpu().numpy().astype(np.int64), w_offs)
+    assert np.array_equal(recs.cpu().numpy()[:w_total], w_recs[:w_total])

@@ -1,0 +1,82 @@
+"""GPU parity of the reduce-then-scan variant, and failure detection: a tile that
+never publishes its status makes its successors' bounded waits run out; the
+kernel reports GB_ERR_TIMEOUT through the sticky device error and returns, and the
+context stays usable.  No fault, trap or hang is involved: the wait limit is a
+few milliseconds of the GPU's global timer."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import stream_compaction_decoupled_gb300 as gb
+from stream_compaction_decoupled_gb300 import workloads
+from parity import as3, assert_scan_matches
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _cuda():
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+    gb.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+@pytest.mark.parametrize("dt", [np.int32, np.float32, np.float64, np.int64])
+@pytest.mark.parametrize("op", ["add", "max", "min"])
+@pytest.mark.parametrize("n", [1, 100, 4096, 4097, 3 * 4096 + 77, 1_000_003])
+def test_rts_matches(dt, op, n):
+    x = (workloads.normal(n, dt, n) if np.dtype(dt).kind == "f"
+         else workloads.small_ints(n, n, -1000, 1000, dtype=dt))
+    xd = dev(x)
+    got = gb.scan_reduce_then_scan(xd, op).cpu().numpy()
+    assert_scan_matches(got, as3(x, 1, n, 1), op, True, what="rts %s %s %d" % (np.dtype(dt).name, op, n))
+    init = x[0] if op != "add" else None
+    got = gb.scan_reduce_then_scan(xd, op, inclusive=False, init=init).cpu().numpy()
+    assert_scan_matches(got, as3(x, 1, n, 1), op, False, init, what="rts excl")
+
+
+def test_rts_full_size_matches_single_pass():
+    w = workloads.BY_NAME["fp32_1e8"]
+    x = w.make()
+    xd = dev(x)
+    got = gb.scan_reduce_then_scan(xd).cpu().numpy()
+    assert_scan_matches(got, as3(x, 1, x.size, 1), "add", True, what="rts fp32 1e8")
+    assert gb.device_error() == gb.OK
+
+
+@pytest.fixture
+def stall():
+    yield
+    gb.set_stalled_tile(-1)
+    gb.set_wait_limit_ns(0)
+
+
+@pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "compact", "pack"])
+def test_stalled_tile_times_out(stall, kind):
+    n = 64 * 4096
+    x = workloads.uniform01(n, np.float32, 1)
+    gb.set_wait_limit_ns(5_000_000)   # 5 ms
+    gb.set_stalled_tile(3)
+    if kind == "rows_f32":
+        gb.scan_inclusive(dev(x))
+    elif kind == "rows_f64":
+        gb.scan_inclusive(dev(x.astype(np.float64)))
+    elif kind == "lanes":
+        gb.scan_inclusive(dev(x), lanes=8)
+    elif kind == "compact":
+        gb.compact(dev(x), "lt", 0.5)
+    else:
+        gb.pack_by_counts(dev((x * 8).astype(np.int32)), 8 * n)
+    assert gb.device_error() == gb.ERR_TIMEOUT
+    # The context is still usable and a normal call is exact again.
+    gb.set_stalled_tile(-1)
+    gb.set_wait_limit_ns(0)
+    xi = workloads.small_ints(n, 2)
+    assert np.array_equal(gb.scan_inclusive(dev(xi)).cpu().numpy(), oracle.scan(xi))
+    assert gb.device_error() == gb.OK
