@@ -233,9 +233,19 @@ def device_error(stream=None) -> int:
     return load().gb_device_error(s)
 
 
+def _event_handle(ev):
+    # torch creates the CUDA event on its first record(); make sure it exists.
+    if ev.cuda_event == 0:
+        ev.record()
+    return ctypes.c_void_p(ev.cuda_event)
+
+
 def set_profile_events(before, after):
-    load().gb_set_profile_events(ctypes.c_void_p(before.cuda_event) if before is not None else None,
-                                 ctypes.c_void_p(after.cuda_event) if after is not None else None)
+    """Have the next calls record `before`/`after` (torch.cuda.Event) around their main kernel."""
+    if before is None or after is None:
+        load().gb_set_profile_events(None, None)
+    else:
+        load().gb_set_profile_events(_event_handle(before), _event_handle(after))
 
 
 def set_wait_limit_ns(ns: int):

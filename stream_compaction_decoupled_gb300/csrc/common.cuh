@@ -233,8 +233,10 @@ __device__ __forceinline__ unsigned lanemask_lt() {
   return m;
 }
 
+// Pause between polls of a tile status: short, because a predecessor that is still
+// X usually publishes within a memory round trip or two.
 __device__ __forceinline__ void backoff(int spins) {
-  __nanosleep(spins < 6 ? (32u << spins) : 2048u);
+  __nanosleep(spins < 3 ? (32u << spins) : 256u);
 }
 
 }  // namespace gbs

@@ -41,7 +41,7 @@ template <class T> __device__ __forceinline__ bool selects(T x, T t, unsigned ma
 }
 
 template <class T>
-__global__ void __launch_bounds__(RowsGeom<T>::NT) compact_kernel(CompactArgs<T> a, PackedStatus<unsigned> st) {
+__global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_kernel(CompactArgs<T> a, PackedStatus<unsigned> st) {
   using G = RowsGeom<T>;
   constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, TILE = G::TILE;
   static_assert(ROUNDS * VEC <= 32, "selection bits must fit one word");
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT) compact_kernel(CompactArgs<T>
     } else {
       if (lane == 0 && !stalled) st.publish(t, FLAG_A, agg);
       bool timed_out;
-      pfx = lookback_warp<unsigned, OP_ADD>(st, 0, t, a.wait_ns, timed_out);
+      pfx = lookback_warp<unsigned, OP_ADD, G::K>(st, 0, t, a.wait_ns, timed_out);
       if (lane == 0) {
         if (!stalled) st.publish(t, FLAG_P, pfx + agg);
         if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);

@@ -32,7 +32,7 @@ struct PackArgs {
   long long stalled_tile;
 };
 
-__global__ void __launch_bounds__(RowsGeom<unsigned>::NT) pack_kernel(PackArgs a, PackedStatus<unsigned> st) {
+__global__ void __launch_bounds__(RowsGeom<unsigned>::NT, RowsGeom<unsigned>::MINB) pack_kernel(PackArgs a, PackedStatus<unsigned> st) {
   using G = RowsGeom<unsigned>;
   constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, TILE = G::TILE;
   __shared__ __align__(128) unsigned s_tile[TILE];
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(RowsGeom<unsigned>::NT) pack_kernel(PackArgs a
     } else {
       if (lane == 0 && !stalled) st.publish(t, FLAG_A, agg);
       bool timed_out;
-      pfx = lookback_warp<unsigned, OP_SATADD>(st, 0, t, a.wait_ns, timed_out);
+      pfx = lookback_warp<unsigned, OP_SATADD, G::K>(st, 0, t, a.wait_ns, timed_out);
       if (lane == 0) {
         if (!stalled) st.publish(t, FLAG_P, Op<unsigned, OP_SATADD>::f(pfx, agg));
         if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);

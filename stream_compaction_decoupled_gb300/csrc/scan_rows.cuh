@@ -37,17 +37,26 @@ template <class T> struct RowsArgs {
   long long stalled_tile;
 };
 
-template <class T> struct RowsGeom {
-  static constexpr int NT = 256;
+// Tile geometry: NT threads, ROUNDS 16-byte vectors per thread, K predecessors
+// per lane in the look-back window, MINB resident CTAs per SM asked of the compiler.
+template <class T, int NT_, int ROUNDS_, int K_, int MINB_> struct RowsCfg {
+  static constexpr int NT = NT_;
   static constexpr int NW = NT / 32;
-  static constexpr int ROUNDS = 4;
+  static constexpr int ROUNDS = ROUNDS_;
   static constexpr int VEC = 16 / (int)sizeof(T);
-  static constexpr int TILE = NW * ROUNDS * 32 * VEC;  // 4096 x 4 B, 2048 x 8 B: 16 KB
+  static constexpr int TILE = NW * ROUNDS * 32 * VEC;
+  static constexpr int K = K_;
+  static constexpr int MINB = MINB_;
 };
 
-template <class T, int OP, class S>
-__global__ void __launch_bounds__(RowsGeom<T>::NT) scan_rows_kernel(RowsArgs<T> a, S st) {
-  using G = RowsGeom<T>;
+// The configuration the library uses: 16 KB tiles of 128 threads, so that a dozen
+// CTAs (tiles) are resident per SM, and a look-back window of 32 x 2 tiles.  (A
+// sweep on the fp32 1e8 scan: windows of 4 or 8 tiles per lane were slower, 6 CTAs
+// of 256 threads were slower, 32 KB tiles were no faster.)
+template <class T> using RowsGeom = RowsCfg<T, 128, 8, 2, 12>;
+
+template <class T, int OP, class G, class S>
+__global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_kernel(RowsArgs<T> a, S st) {
   constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, TILE = G::TILE;
   __shared__ __align__(128) T s_tile[TILE];
   __shared__ __align__(8) unsigned long long s_bar;
@@ -117,7 +126,7 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT) scan_rows_kernel(RowsArgs<T> 
     } else {
       if (lane == 0 && !stalled) st.publish(first + tt, FLAG_A, agg);
       bool timed_out;
-      const T pfx = lookback_warp<T, OP>(st, first, tt, a.wait_ns, timed_out);
+      const T pfx = lookback_warp<T, OP, G::K>(st, first, tt, a.wait_ns, timed_out);
       if (lane == 0) {
         if (!stalled) st.publish(first + tt, FLAG_P, Op<T, OP>::f(pfx, agg));
         s_prefix = pfx;
@@ -168,8 +177,8 @@ template <class T> size_t rows_reset_bytes(unsigned num_tiles) {
   return kHeaderBytes + round_up((size_t)num_tiles * 4, 256);
 }
 
-template <class T> unsigned rows_tiles(long long B, long long R) {
-  const long long tpr = (R + RowsGeom<T>::TILE - 1) / RowsGeom<T>::TILE;
+template <class T, class G = RowsGeom<T>> unsigned rows_tiles(long long B, long long R) {
+  const long long tpr = (R + G::TILE - 1) / G::TILE;
   return (unsigned)(B * tpr);
 }
 
@@ -188,15 +197,14 @@ template <class T> typename StatusFor<T>::type rows_status(void* temp, unsigned 
   return st;
 }
 
-template <class T, int OP>
+template <class T, int OP, class G = RowsGeom<T>>
 cudaError_t launch_rows_op(const ScanJob& job, const LaunchCtx& ctx) {
-  using G = RowsGeom<T>;
   RowsArgs<T> a;
   a.in = (const T*)job.in;
   a.out = (T*)job.out;
   a.R = job.R;
   a.tiles_per_row = (unsigned)((job.R + G::TILE - 1) / G::TILE);
-  a.num_tiles = rows_tiles<T>(job.B, job.R);
+  a.num_tiles = rows_tiles<T, G>(job.B, job.R);
   a.counter = (unsigned*)job.temp;
   a.err = ctx.err;
   a.init = T{};
@@ -210,7 +218,7 @@ cudaError_t launch_rows_op(const ScanJob& job, const LaunchCtx& ctx) {
   cudaError_t e = cudaMemsetAsync(job.temp, 0, rows_reset_bytes<T>(a.num_tiles), ctx.stream);
   if (e != cudaSuccess) return e;
   profile_before(ctx);
-  scan_rows_kernel<T, OP, decltype(st)><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
+  scan_rows_kernel<T, OP, G, decltype(st)><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
   profile_after(ctx);
   return cudaGetLastError();
 }

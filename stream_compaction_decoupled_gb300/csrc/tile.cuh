@@ -64,20 +64,26 @@ template <class T> struct StatusFor {
 
 // ---- decoupled look-back -------------------------------------------------------------
 
-// Warp-cooperative look-back (The CUDA Handbook, 13.3.4, Figure 13-11): lane k
-// inspects predecessor frontier-k, so the warp reads the 32 nearest predecessors
-// at once; it re-reads while a tile it still needs is X; a ballot finds the
-// nearest P; the values from the frontier back to that P are combined in tile
-// order (earlier tiles on the left); with no P in the window, all 32 aggregates
-// are combined and the warp steps back 32 tiles.  A tile only needs its window up
-// to the nearest P to be non-X, not the whole window.
+// Warp-cooperative look-back (The CUDA Handbook, 13.3.4, Figure 13-11), widened:
+// lane l inspects the K predecessors frontier-K*l-i (i = 0..K-1, nearest first), so
+// one round trip covers a window of 32*K tiles instead of 32.  A ballot finds the
+// lane holding the nearest P; the values from the frontier back to that P are
+// combined in tile order (earlier tiles on the left); with no P in the window all
+// 32*K aggregates are combined and the warp steps back a whole window.  A tile only
+// needs the part of its window up to the nearest P to be non-X.
+//
+// The window is read once; while it is not ready, only the entries that are still
+// X and nearer than the nearest P are read again (an A or P already seen stays
+// valid: an aggregate never changes, and any P is a correct inclusive prefix).  So
+// a waiting warp costs the memory system a few words per poll, not its window:
+// with hundreds of tiles resident per GPU, re-reading whole windows floods L2.
 //
 // `first` is the status index of tile 0 of this row (whose status is always P),
 // `tt` >= 1 the tile's index within the row.  Called by all 32 lanes of one warp;
 // returns the tile's exclusive prefix in every lane.  Every wait is bounded by
 // wait_ns of global time; on expiry *timed_out is set and whatever was read is
 // returned.
-template <class T, int OP, class S>
+template <class T, int OP, int K, class S>
 __device__ __forceinline__ T lookback_warp(const S& st, long long first, long long tt,
                                            unsigned long long wait_ns, bool& timed_out) {
   const int lane = threadIdx.x & 31;
@@ -86,17 +92,34 @@ __device__ __forceinline__ T lookback_warp(const S& st, long long first, long lo
   bool have = false;
   timed_out = false;
   for (;;) {
-    const long long p = frontier - lane;
-    unsigned f = FLAG_P;
-    T v{};
+    unsigned f[K];
+    T v[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      const long long p = frontier - (long long)K * lane - i;
+      v[i] = T{};
+      f[i] = (p >= 0) ? st.poll(first + p, v[i]) : FLAG_P;  // before the row: stops the walk
+    }
+    int fp = K;        // this lane's nearest P (K: none)
+    int nearest = 32;  // lane holding the window's nearest P (32: none)
     int spins = 0;
     unsigned long long t0 = 0;
     for (;;) {
-      f = (p >= 0) ? st.poll(first + p, v) : FLAG_P;  // before the row: stops the walk
-      const unsigned pm = __ballot_sync(0xffffffffu, f == FLAG_P);
-      const unsigned xm = __ballot_sync(0xffffffffu, f == FLAG_X);
-      const unsigned need = pm ? (pm ^ (pm - 1u)) : 0xffffffffu;  // lanes 0..nearest P
-      if ((xm & need) == 0) break;
+      fp = K;
+#pragma unroll
+      for (int i = K - 1; i >= 0; --i)
+        if (f[i] == FLAG_P) fp = i;
+      bool x_before_p = false, any_x = false;
+#pragma unroll
+      for (int i = 0; i < K; ++i)
+        if (f[i] == FLAG_X) {
+          any_x = true;
+          if (i < fp) x_before_p = true;
+        }
+      const unsigned pm = __ballot_sync(0xffffffffu, fp < K);
+      nearest = pm ? __ffs(pm) - 1 : 32;
+      const bool bad = (lane < nearest && any_x) || (lane == nearest && x_before_p);
+      if (!__any_sync(0xffffffffu, bad)) break;
       // The time-out decision is taken by the whole warp at once, so no lane leaves
       // the loop while others still poll (the ballots above need every lane).
       if (spins == 0) t0 = __shfl_sync(0xffffffffu, globaltimer(), 0);
@@ -106,23 +129,43 @@ __device__ __forceinline__ T lookback_warp(const S& st, long long first, long lo
         break;
       }
       backoff(spins++);
+      // Re-read only the blocking entries.
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const bool needed = lane < nearest || (lane == nearest && i < fp);
+        if (needed && f[i] == FLAG_X) {
+          const long long p = frontier - (long long)K * lane - i;
+          f[i] = (p >= 0) ? st.poll(first + p, v[i]) : FLAG_P;
+        }
+      }
     }
-    const unsigned pm = __ballot_sync(0xffffffffu, f == FLAG_P);
-    const int nearest = pm ? __ffs(pm) - 1 : 32;
-    const int m = nearest < 32 ? nearest : 31;
-    if (lane <= m && p >= 0) v = st.fetch(first + p, f, v);
-    // Ordered combination of lanes 0..m (lane k = tile frontier-k).
+    // This lane's contribution: its tiles from its nearest P (or its farthest tile)
+    // down to the nearest one, in tile order.
+    const int m = lane == nearest ? fp : K - 1;
+    T w{};
+    if (lane <= nearest) {
+#pragma unroll
+      for (int i = K - 1; i >= 0; --i) {
+        if (i <= m) {
+          const long long p = frontier - (long long)K * lane - i;
+          const T val = p >= 0 ? st.fetch(first + p, f[i], v[i]) : v[i];
+          w = (i == m) ? val : Op<T, OP>::f(w, val);
+        }
+      }
+    }
+    // Ordered combination of lanes 0..min(nearest, 31) (lane k holds later tiles than k+1).
+    const int last = nearest < 32 ? nearest : 31;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      T o = __shfl_down_sync(0xffffffffu, v, off);
-      if (lane + off <= m) v = Op<T, OP>::f(o, v);
+      T o = __shfl_down_sync(0xffffffffu, w, off);
+      if (lane + off <= last) w = Op<T, OP>::f(o, w);
     }
-    v = __shfl_sync(0xffffffffu, v, 0);
-    acc = have ? Op<T, OP>::f(v, acc) : v;
+    w = __shfl_sync(0xffffffffu, w, 0);
+    acc = have ? Op<T, OP>::f(w, acc) : w;
     have = true;
     timed_out = __any_sync(0xffffffffu, timed_out);
     if (nearest < 32 || timed_out) break;
-    frontier -= 32;
+    frontier -= 32LL * K;
   }
   return acc;
 }
