@@ -160,6 +160,28 @@ int gb_scan_reduce_then_scan(int dtype, int op, int inclusive, const void* in, v
                              void* stream);
 
 /*
+ * Inclusive scan that allocates nothing, for callers that cannot call cudaMalloc or
+ * cudaMallocAsync (code running under an allocator it does not own, or that must not
+ * grow the process's device memory after start-up).  The pages have no counterpart:
+ * their host functions draw scratch from the stream-ordered allocator.
+ *   dtype, op       as gb_scan_inclusive; one lane per element (lanes = 1)
+ *   in, out, n      device pointers and element count, as gb_scan_inclusive
+ *   stream          cudaStream_t as void*
+ * The scratch (tile counter and tile-status words) is one static device array of
+ * 1 MiB (1048576 bytes) inside the library, held by every GPU that loads the library
+ * until the process exits.  Sizes whose scratch does not fit
+ * (gb_temp_storage_bytes(GB_KIND_SCAN, dtype, 1, n, 0) > 1048576: n above
+ * 536,739,840 for 4-byte types, above 107,347,968 for 8-byte types) are rejected
+ * with GB_ERR_RANGE before anything is enqueued.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current; make
+ * that first call before any stream capture.  Every call shares the array and clears
+ * what must start at zero on `stream`; calls that can overlap on the GPU (different
+ * streams without ordering, or concurrent host threads) race on it.
+ * Errors: as gb_scan_inclusive, plus GB_ERR_RANGE for the size limit.
+ */
+int gb_scan_inclusive_noalloc(int dtype, int op, const void* in, void* out, int64_t n, void* stream);
+
+/*
  * Scratch bytes a call needs for the given kind and sizes (rows = n for the 1-D
  * kinds; cols ignored there).  Returns 0 for an invalid combination.
  */

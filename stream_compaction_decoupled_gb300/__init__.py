@@ -45,6 +45,7 @@ SIGNATURES = {
     "gb_set_profile_events": (None, [_vp, _vp]),
     "gb_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "gb_set_stalled_tile": (None, [_i64]),
+    "gb_scan_inclusive_noalloc": (_i, [_i, _i, _vp, _vp, _i64, _vp]),
 }
 
 _lib = None
