@@ -5,15 +5,28 @@
 
 #include "scan_lanes.cuh"
 #include "scan_rows.cuh"
+#include "scan_stash.cuh"
 
 namespace gbs {
 
 template <class T> size_t scan_temp_bytes(long long B, long long R, long long C) {
-  if (C == 1) return kHeaderBytes + rows_status_bytes<T>(rows_tiles<T>(B, R));
+  if (C == 1) {
+    // Either kernel may run (the choice depends on the pointers' alignment).
+    const size_t rows = kHeaderBytes + rows_status_bytes<T>(rows_tiles<T>(B, R));
+    const size_t stash = B == 1 ? kHeaderBytes + stash_status_bytes<T>(R) : 0;
+    return rows > stash ? rows : stash;
+  }
   return lanes_temp_bytes<T>(B, R, C);
 }
 
 template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& ctx) {
+  if (job.C == 1 && stash_applies<T>(job, ctx.num_sms)) {
+    switch (job.op) {
+      case OP_ADD: return launch_stash_op<T, OP_ADD>(job, ctx);
+      case OP_MAX: return launch_stash_op<T, OP_MAX>(job, ctx);
+      default: return launch_stash_op<T, OP_MIN>(job, ctx);
+    }
+  }
   if (job.C == 1) {
     switch (job.op) {
       case OP_ADD: return launch_rows_op<T, OP_ADD>(job, ctx);

@@ -304,6 +304,64 @@ __device__ __forceinline__ void tile_apply_pass(uint4* run, int lane, const T (&
   }
 }
 
+// The same two passes on a tile held in registers: x[j] is the thread's 16-byte
+// vector of round j (vector index (warp*ROUNDS + j)*32 + lane of the tile).
+template <class T, int OP, int ROUNDS>
+__device__ __forceinline__ T regs_reduce_pass(const Vec<T> (&x)[ROUNDS], int lane, T (&pre)[ROUNDS]) {
+  constexpr int VEC = Vec<T>::N;
+  T carry{};
+#pragma unroll
+  for (int j = 0; j < ROUNDS; ++j) {
+    T t = x[j].v[0];
+#pragma unroll
+    for (int e = 1; e < VEC; ++e) t = Op<T, OP>::f(t, x[j].v[e]);
+    const T wi = warp_inclusive<T, OP>(t, lane);
+    const T we = __shfl_up_sync(0xffffffffu, wi, 1);
+    const T rt = __shfl_sync(0xffffffffu, wi, 31);
+    if (j == 0) {
+      pre[0] = we;
+      carry = rt;
+    } else {
+      pre[j] = lane == 0 ? carry : Op<T, OP>::f(carry, we);
+      carry = Op<T, OP>::f(carry, rt);
+    }
+  }
+  return carry;
+}
+
+template <class T, int OP, int ROUNDS>
+__device__ __forceinline__ void regs_apply_pass(Vec<T> (&x)[ROUNDS], int lane, const T (&pre)[ROUNDS], T base,
+                                                bool has_base, bool inclusive) {
+  constexpr int VEC = Vec<T>::N;
+#pragma unroll
+  for (int j = 0; j < ROUNDS; ++j) {
+    T r;
+    bool h;
+    if (j > 0 || lane > 0) {
+      r = has_base ? Op<T, OP>::f(base, pre[j]) : pre[j];
+      h = true;
+    } else {
+      r = base;
+      h = has_base;
+    }
+    if (inclusive) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        r = h ? Op<T, OP>::f(r, x[j].v[e]) : x[j].v[e];
+        h = true;
+        x[j].v[e] = r;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const T xv = x[j].v[e];
+        x[j].v[e] = r;
+        r = Op<T, OP>::f(r, xv);
+      }
+    }
+  }
+}
+
 // Block scan of the NW warp totals by warp 0 (The CUDA Handbook, 13.3.1, Listing
 // 13-5, with one shared slot per warp as in AcceleratedKernels.jl PR #208): on
 // return s_warp[w] holds the inclusive total of warps 0..w; returns the tile

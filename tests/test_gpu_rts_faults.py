@@ -57,9 +57,9 @@ def stall():
     gb.set_wait_limit_ns(0)
 
 
-@pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "compact", "pack"])
+@pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "compact", "pack", "l2_resident"])
 def test_stalled_tile_times_out(stall, kind):
-    n = 64 * 4096
+    n = 64 * 4096 if kind != "l2_resident" else 12_000_000
     x = workloads.uniform01(n, np.float32, 1)
     gb.set_wait_limit_ns(5_000_000)   # 5 ms
     gb.set_stalled_tile(3)
@@ -69,6 +69,8 @@ def test_stalled_tile_times_out(stall, kind):
         gb.scan_inclusive(dev(x.astype(np.float64)))
     elif kind == "lanes":
         gb.scan_inclusive(dev(x), lanes=8)
+    elif kind == "l2_resident":  # one long row: the stalled index is a run of 4 tiles
+        gb.scan_inclusive(dev(x))
     elif kind == "compact":
         gb.compact(dev(x), "lt", 0.5)
     else:

@@ -176,3 +176,34 @@ def test_full_size_workload(name):
         assert_scan_matches(got, as3(x, 1, x.size, 1), "max", False, x[0], what=name + " excl")
     del xd
     assert gb.device_error() == gb.OK
+
+
+# ---- the L2-resident single-pass path (one long aligned row) ----------------------
+# It applies from 152 SMs x 4 tiles x 4 runs upwards: 9,961,472 four-byte or
+# 4,980,736 eight-byte elements.
+
+@pytest.mark.parametrize("dt,n", [("f32", 9_961_472), ("f32", 9_961_472 + 77), ("f32", 33_554_432 + 5),
+                                  ("i32", 12_000_001), ("u32", 10_000_000), ("f64", 4_980_736 + 1),
+                                  ("i64", 7_000_003), ("f64", 16_777_216)])
+@pytest.mark.parametrize("op", ["add", "max", "min"])
+def test_l2_resident_path(dt, n, op):
+    if dt not in DTYPES:
+        pytest.skip("no torch dtype")
+    x = make(dt, n, n % 1000)
+    xd = to_dev(x)
+    got = to_host(gb.scan_inclusive(xd, op))
+    assert_scan_matches(got, as3(x, 1, n, 1), op, True, what="%s %s incl n=%d" % (dt, op, n))
+    init = x[0] if op != "add" else None
+    got = to_host(gb.scan_exclusive(xd, op, init=init))
+    assert_scan_matches(got, as3(x, 1, n, 1), op, False, init, what="%s %s excl n=%d" % (dt, op, n))
+    assert gb.device_error() == gb.OK
+
+
+def test_l2_resident_path_repeated_in_place():
+    x = workloads.small_ints(20_000_000, 5, -3, 4)
+    want = oracle.scan(x)
+    for _ in range(5):
+        y = to_dev(x)
+        gb.scan_inclusive(y, out=y)
+        assert np.array_equal(to_host(y), want)
+    assert gb.device_error() == gb.OK
