@@ -216,7 +216,7 @@ def time_call(fn, reps: int, flush, stream, kernel_events: bool):
             "step_ms_median": float(np.median(steps))}
 
 
-def secondary_workloads(device, hbm_peak, reps=10):
+def secondary_workloads(device, hbm_peak, reps=10, only=None):
     """Every other workload: kernel time, GB/s, fraction of the HBM roofline."""
     import torch
     import stream_compaction_decoupled_gb300 as gb
@@ -225,7 +225,7 @@ def secondary_workloads(device, hbm_peak, reps=10):
     flush = L2Flush(device)
     out = {}
     for w in W.WORKLOADS:
-        if w.name == HEADLINE:
+        if w.name == HEADLINE or (only and w.name not in only):
             continue
         x = torch.from_numpy(w.make()).to(device)
         es = x.element_size()
@@ -269,6 +269,8 @@ def secondary_workloads(device, hbm_peak, reps=10):
                        "throughput": round(units / (ms * 1e-3) / 1e9, 3), "throughput_unit": unit,
                        "algorithmic_bytes": int(nbytes), "l2": "flushed between repetitions"}
         del x
+    if only and "fp32_1e8_reduce_then_scan" not in only:
+        return out
     # The reduce-then-scan comparison variant on the headline workload.
     xh = torch.from_numpy(W.BY_NAME[HEADLINE].make()).to(device)
     yh = torch.empty_like(xh)
@@ -399,7 +401,7 @@ def our_arm(args, rank, world, local_rank):
 
     extra = None
     if rank == 0 and not args.headline_only and world == 1 and n == N_HEAD:
-        extra = secondary_workloads(device, hbm_peak)
+        extra = secondary_workloads(device, hbm_peak, only=set(args.workloads.split(",")) if args.workloads else None)
     if rank == 0:
         sampler.stop()
 
@@ -464,6 +466,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default="",
+                    help="comma-separated names of the other workloads to time (default: all)")
     ap.add_argument("--n", type=int, default=N_HEAD,
                     help="headline size (default 1e8); smaller values are for profiling runs only")
     args = ap.parse_args(argv)

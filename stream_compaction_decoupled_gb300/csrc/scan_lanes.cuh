@@ -36,21 +36,21 @@ template <class T> struct LanesArgs {
   long long stalled_tile;
 };
 
-template <class T> struct LanesGeom {
+template <class T, int RPG_ = (sizeof(T) == 4 ? 16 : 8)> struct LanesGeomT {
   static constexpr int NT = 256;
   static constexpr int NW = NT / 32;
-  static constexpr int RPG = sizeof(T) == 4 ? 16 : 8;  // rows per thread
-  static constexpr int CTMAX = sizeof(T) == 4 ? 64 : 32; // 256-byte strips
+  static constexpr int RPG = RPG_;                        // rows per thread
+  static constexpr int CTMAX = sizeof(T) == 4 ? 64 : 32;  // 256-byte strips
   static int ct(long long C) { return C <= CTMAX ? (int)C : CTMAX; }
   static int groups(int CT) {
     int g = NT / CT;
     return g > 32 ? 32 : g;
   }
 };
+template <class T> using LanesGeom = LanesGeomT<T>;
 
-template <class T, int OP, class S>
-__global__ void __launch_bounds__(LanesGeom<T>::NT) scan_lanes_kernel(LanesArgs<T> a, S st) {
-  using Gm = LanesGeom<T>;
+template <class T, int OP, class S, class Gm = LanesGeom<T>>
+__global__ void __launch_bounds__(Gm::NT) scan_lanes_kernel(LanesArgs<T> a, S st) {
   constexpr int NT = Gm::NT, NW = Gm::NW, RPG = Gm::RPG;
   __shared__ __align__(128) T s_tile[NT * RPG];
   __shared__ T s_gx[NT];     // group totals, then exclusive group prefixes, [g*CT + c]
@@ -222,14 +222,13 @@ __global__ void __launch_bounds__(LanesGeom<T>::NT) scan_lanes_kernel(LanesArgs<
   }
 }
 
-template <class T> struct LanesPlan {
+template <class T, class Gm = LanesGeom<T>> struct LanesPlan {
   int CT, G, RT;
   unsigned strips, tiles_per_chain, num_tiles;
 };
 
-template <class T> LanesPlan<T> lanes_plan(long long B, long long R, long long C) {
-  using Gm = LanesGeom<T>;
-  LanesPlan<T> p;
+template <class T, class Gm = LanesGeom<T>> LanesPlan<T, Gm> lanes_plan(long long B, long long R, long long C) {
+  LanesPlan<T, Gm> p;
   p.CT = Gm::ct(C);
   p.G = Gm::groups(p.CT);
   p.RT = p.G * Gm::RPG;
@@ -244,24 +243,23 @@ template <class T> size_t lanes_init_bytes(long long C) {
   const long long n = C < 4096 ? C : 4096;
   return round_up((size_t)n * sizeof(T), 256);
 }
-template <class T> size_t lanes_status_entries(const LanesPlan<T>& p) {
+template <class T, class Gm> size_t lanes_status_entries(const LanesPlan<T, Gm>& p) {
   return (size_t)p.num_tiles * p.CT;
 }
-template <class T> size_t lanes_flag_bytes(const LanesPlan<T>& p) {
+template <class T, class Gm> size_t lanes_flag_bytes(const LanesPlan<T, Gm>& p) {
   return sizeof(T) == 4 ? round_up(lanes_status_entries(p) * 8, 256)
                         : round_up(lanes_status_entries(p) * 4, 256);
 }
-template <class T> size_t lanes_temp_bytes(long long B, long long R, long long C) {
-  const LanesPlan<T> p = lanes_plan<T>(B, R, C);
+template <class T, class Gm = LanesGeom<T>> size_t lanes_temp_bytes(long long B, long long R, long long C) {
+  const LanesPlan<T, Gm> p = lanes_plan<T, Gm>(B, R, C);
   size_t s = kHeaderBytes + lanes_init_bytes<T>(C) + lanes_flag_bytes(p);
   if (sizeof(T) == 8) s += 2 * round_up(lanes_status_entries(p) * sizeof(T), 256);
   return s;
 }
 
-template <class T, int OP>
+template <class T, int OP, class Gm = LanesGeom<T>>
 cudaError_t launch_lanes_op(const ScanJob& job, const LaunchCtx& ctx) {
-  using Gm = LanesGeom<T>;
-  const LanesPlan<T> p = lanes_plan<T>(job.B, job.R, job.C);
+  const LanesPlan<T, Gm> p = lanes_plan<T, Gm>(job.B, job.R, job.C);
   LanesArgs<T> a;
   a.in = (const T*)job.in;
   a.out = (T*)job.out;
@@ -298,7 +296,7 @@ cudaError_t launch_lanes_op(const ScanJob& job, const LaunchCtx& ctx) {
                         cudaMemcpyHostToDevice, ctx.stream);
   if (e != cudaSuccess) return e;
   profile_before(ctx);
-  scan_lanes_kernel<T, OP, decltype(st)><<<p.num_tiles, Gm::NT, 0, ctx.stream>>>(a, st);
+  scan_lanes_kernel<T, OP, decltype(st), Gm><<<p.num_tiles, Gm::NT, 0, ctx.stream>>>(a, st);
   profile_after(ctx);
   return cudaGetLastError();
 }

@@ -570,6 +570,10 @@ template <class T> size_t stash_reset_bytes(long long n) {
 // When the L2-resident scan applies: one row, 16-byte aligned data, and enough
 // tiles that the persistent grid has work for every SM.
 template <class T> bool stash_applies(const ScanJob& job, int num_sms) {
+  // Not for fp64: there the arithmetic, not HBM, is the limit (GB300 adds fp64 at a
+  // small fraction of its fp32 rate), and the extra reduction would cost one more
+  // add per element.
+  if (std::is_same<T, double>::value) return false;
   return job.B == 1 && job.C == 1 && (uintptr_t)job.in % 16 == 0 && (uintptr_t)job.out % 16 == 0 &&
          job.R >= (long long)num_sms * StashCfg<T>::TILE * StashCfg<T>::RUN * 4;
 }

@@ -362,6 +362,42 @@ __device__ __forceinline__ void regs_apply_pass(Vec<T> (&x)[ROUNDS], int lane, c
   }
 }
 
+// ---- thread-contiguous chunks (for operators that are costly per element) ------------
+
+// Each thread owns CV consecutive 16-byte vectors of the tile (its "chunk").  A warp
+// reading vector k of every lane's chunk would hit one bank group 8 times over, so
+// lane l reads its vectors in the rotated order (j + l) mod CV: conflict-free.  The
+// rotation is undone in registers with log2(CV) select stages before the ordered
+// scan, and redone before the write-back.  Costs a few integer selects per element
+// and saves the warp scans: one warp scan per CV*VEC elements instead of per VEC.
+template <class T, int CV>
+__device__ __forceinline__ void chunk_load(const uint4* chunk, int lane, Vec<T> (&v)[CV]) {
+#pragma unroll
+  for (int j = 0; j < CV; ++j) v[j] = ld_vec<T>(chunk + ((j + lane) & (CV - 1)));
+}
+template <class T, int CV>
+__device__ __forceinline__ void chunk_store(uint4* chunk, int lane, const Vec<T> (&v)[CV]) {
+#pragma unroll
+  for (int j = 0; j < CV; ++j) st_vec<T>(chunk + ((j + lane) & (CV - 1)), v[j]);
+}
+// w[k] = v[(k - rot) mod CV] (dir = -1) or v[(k + rot) mod CV] (dir = +1).
+template <class T, int CV, int DIR>
+__device__ __forceinline__ void chunk_rotate(Vec<T> (&v)[CV], int rot) {
+#pragma unroll
+  for (int s = 1; s < CV; s <<= 1) {
+    const bool b = (rot & s) != 0;
+    Vec<T> t[CV];
+#pragma unroll
+    for (int k = 0; k < CV; ++k) {
+      const Vec<T>& src = v[(k + DIR * s + CV) & (CV - 1)];
+#pragma unroll
+      for (int e = 0; e < Vec<T>::N; ++e) t[k].v[e] = b ? src.v[e] : v[k].v[e];
+    }
+#pragma unroll
+    for (int k = 0; k < CV; ++k) v[k] = t[k];
+  }
+}
+
 // Block scan of the NW warp totals by warp 0 (The CUDA Handbook, 13.3.1, Listing
 // 13-5, with one shared slot per warp as in AcceleratedKernels.jl PR #208): on
 // return s_warp[w] holds the inclusive total of warps 0..w; returns the tile
