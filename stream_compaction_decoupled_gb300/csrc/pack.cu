@@ -6,10 +6,10 @@
 // Per tile of 4096 counts (row-scan geometry, claimed in order): bulk-copy the
 // counts into shared memory; exclusive-scan them there (pass 1, block scan,
 // decoupled look-back over packed (flag, running total) words, pass 2); write the
-// global start offsets if asked; then emit the tile's records contiguously: thread
-// k of the CTA takes output slots k, k+256, ... of the tile's run and finds the
-// object owning each slot by a binary search over the tile's local offsets, so
-// the record stores are coalesced whatever the count distribution.  Offsets add
+// global start offsets if asked; then emit the tile's records contiguously: each
+// thread takes runs of consecutive output slots of the tile, finds the object owning
+// the first by a binary search over the tile's local offsets and walks forward, so
+// the work per record is constant whatever the count distribution.  Offsets add
 // with saturation at 2^31 so a total that does not fit int32 is caught, not
 // wrapped.
 #include "scan_rows.cuh"
@@ -153,17 +153,27 @@ __global__ void __launch_bounds__(RowsGeom<unsigned>::NT, RowsGeom<unsigned>::MI
   __syncthreads();
 
   // Emit the tile's records: output slot j of the tile belongs to the last object
-  // whose local offset is <= j.
-  for (unsigned j = tid; j < agg; j += NT) {
-    const long long pos = (long long)pfx + j;
-    if (pos >= a.capacity) break;
+  // whose local offset is <= j.  Each thread takes V consecutive slots per round: one
+  // binary search for its first slot, then a forward walk (objects with no records
+  // share their successor's offset and are stepped over).
+  constexpr int V = 32;
+  for (unsigned base = 0; base < agg; base += NT * V) {
+    const unsigned j0 = base + (unsigned)tid * V;
+    if (j0 >= agg) continue;
     int lo = 0, hi = len;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (s_tile[mid] <= j) lo = mid + 1;
+      if (s_tile[mid] <= j0) lo = mid + 1;
       else hi = mid;
     }
-    a.records[pos] = (int)(off + lo - 1);
+    int obj = lo - 1;
+    const unsigned jend = j0 + V < agg ? j0 + V : agg;
+    for (unsigned j = j0; j < jend; ++j) {
+      while (obj + 1 < len && s_tile[obj + 1] <= j) ++obj;
+      const long long pos = (long long)pfx + j;
+      if (pos >= a.capacity) break;
+      a.records[pos] = (int)(off + obj);
+    }
   }
 }
 

@@ -4,10 +4,11 @@
 // lanes, a dual number with 16 partials is 17 fp64 lanes), each lane on its own.
 //
 // A tile is RT consecutive positions (rows) x CT consecutive lanes (a strip of the
-// columns; CT = C when C is small).  Its size is chosen from the element size so
-// that it stays near 16 KB whatever the lane count, which is what lets 96- and
-// 136-byte elements fit shared memory with many CTAs per SM (AcceleratedKernels.jl
-// PR #208 sizes its tiles from the element type for the same reason).  Threads map
+// columns; CT = C when C is small).  Its row count is chosen from the lane count so
+// that its size stays fixed (32 KB for 4-byte, 64 KB for 8-byte lanes) whatever the
+// element width, which is what lets 96- and 136-byte elements fit shared memory
+// (AcceleratedKernels.jl PR #208 sizes its tiles from the element type for the same
+// reason).  Threads map
 // to (lane c, row group g); each thread combines RPG rows of one lane serially in
 // shared memory, a warp scans the G group totals of a lane, and one thread per
 // lane looks back along that lane.  Tiles of one (batch, strip) chain are scanned
@@ -36,7 +37,12 @@ template <class T> struct LanesArgs {
   long long stalled_tile;
 };
 
-template <class T, int RPG_ = (sizeof(T) == 4 ? 16 : 8)> struct LanesGeomT {
+// Rows per thread: 32 (tiles of 32 KB for 4-byte and 64 KB for 8-byte lanes).  A
+// sweep over 8..64 rows per thread on the column and lane-vector workloads (4096x4096
+// and 1e6x8 axis 0, 96-byte structs, 17-lane duals, 1000x1e4 fp64 axis 0) put 32 at
+// or near the best everywhere: fewer, larger tiles mean fewer look-backs along a
+// chain, which is what limits these scans (dual16 1e6: 372 us at 8, 165 us at 32).
+template <class T, int RPG_ = 32> struct LanesGeomT {
   static constexpr int NT = 256;
   static constexpr int NW = NT / 32;
   static constexpr int RPG = RPG_;                        // rows per thread
