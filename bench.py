@@ -400,7 +400,7 @@ def our_arm(args, rank, world, local_rank):
     barrier(device)
 
     extra = None
-    if rank == 0 and not args.headline_only and world == 1 and n == N_HEAD:
+    if rank == 0 and not args.headline_only and world == 1 and (n == N_HEAD or args.workloads):
         extra = secondary_workloads(device, hbm_peak, only=set(args.workloads.split(",")) if args.workloads else None)
     if rank == 0:
         sampler.stop()
