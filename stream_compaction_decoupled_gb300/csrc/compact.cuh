@@ -17,6 +17,7 @@
 
 #include "launch.h"
 #include "scan_rows.cuh"
+#include "scan_seg.cuh"
 
 namespace gbs {
 
@@ -148,18 +149,164 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_ke
   for (unsigned k = tid; k < cnt; k += NT) dst[k] = s_idx[k];
 }
 
+// The same selection for inputs that fit in L2, with the three phases of the
+// segment scan (scan_seg.cuh): count per warp part, publish segment counts and
+// gather the earlier ones, rescan from L2 and write the indices.  Within a round,
+// a lane's selected elements get consecutive output slots after those of the
+// lanes before it (one ballot per vector slot), so every store of a round lands in
+// one window of at most 32 x VEC indices.
+template <class T> struct CompactSegArgs : SegArgsBase {
+  const T* in;
+  T thr;
+  unsigned predmask;
+  int* out_idx;
+  int* out_count;
+};
+
+template <class T, class G>
+__global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegArgs<T> a, PackedStatus<unsigned> st) {
+  constexpr int NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, CH = G::CH;
+  __shared__ unsigned s_seg;
+  __shared__ unsigned s_warp[NW];
+  __shared__ unsigned s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
+  __syncthreads();
+  const unsigned seg = s_seg;
+  long long c0, c1;
+  seg_chunks(a, seg, warp, NW, c0, c1);
+
+  // Phase 1: selected elements in the warp's part (coalesced vectors, U per lane in
+  // flight, L2 evict-last so that phase 3 finds them).
+  unsigned cnt = 0;
+  {
+    constexpr int U = 8;
+    const unsigned long long keep = l2_policy_evict_last();
+    const long long e1 = c1 * CH < a.n ? c1 * CH : a.n;
+    const long long v1 = e1 / VEC;
+    const uint4* p = reinterpret_cast<const uint4*>(a.in);
+    long long v = c0 * CH / VEC + lane;
+    for (; v + 32 * (U - 1) < v1; v += 32 * U) {
+      uint4 u[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        Vec<T> x;
+        memcpy(x.v, &u[k], 16);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) cnt += selects(x.v[e], a.thr, a.predmask) ? 1u : 0u;
+      }
+    }
+    for (; v < v1; v += 32) {
+      const uint4 u = ld_hint(p + v, keep);
+      Vec<T> x;
+      memcpy(x.v, &u, 16);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) cnt += selects(x.v[e], a.thr, a.predmask) ? 1u : 0u;
+    }
+    if (lane == 0)
+      for (long long i = v1 * VEC; i < e1; ++i) cnt += selects(a.in[i], a.thr, a.predmask) ? 1u : 0u;
+  }
+  cnt = __reduce_add_sync(0xffffffffu, cnt);
+  if (lane == 0) s_warp[warp] = cnt;
+  __syncthreads();
+
+  // Phase 2: publish the segment's count, gather the earlier counts.
+  if (warp == 0) {
+    const unsigned agg = block_scan_warp_totals<unsigned, OP_ADD, NW>(s_warp, lane);
+    if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
+    unsigned base = 0;
+    if (seg > 0) {
+      bool timed_out;
+      base = seg_gather<unsigned, OP_ADD, G::M>(st, seg, a.wait_ns, timed_out);
+      if (lane == 0 && timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+    }
+    if (lane == 0) {
+      s_base = base;
+      if (seg == a.ctas - 1) *a.out_count = (int)(base + agg);
+    }
+  }
+  __syncthreads();
+
+  // Phase 3: rescan from L2 and write the selected indices.
+  unsigned off = s_base + (warp > 0 ? s_warp[warp - 1] : 0u);
+  const unsigned long long drop = l2_policy_evict_first();
+  const unsigned lt = lanemask_lt();
+  Vec<T> x[ROUNDS];
+  if (c0 < c1) seg_load<T, ROUNDS>(x, a.in, c0 * CH, a.n, lane, drop);
+  for (long long c = c0; c < c1; ++c) {
+    Vec<T> y[ROUNDS];  // the next chunk, requested before this one is processed
+    if (c + 1 < c1) seg_load<T, ROUNDS>(y, a.in, (c + 1) * CH, a.n, lane, drop);
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+      const long long p0 = c * CH + (long long)(j * 32 + lane) * VEC;
+      unsigned sel = 0, before = 0, total = 0;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const bool s = p0 + e < a.n && selects(x[j].v[e], a.thr, a.predmask);
+        const unsigned bal = __ballot_sync(0xffffffffu, s);
+        before += __popc(bal & lt);
+        total += __popc(bal);
+        sel |= (unsigned)s << e;
+      }
+      int* dst = a.out_idx + off + before;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e)
+        if ((sel >> e) & 1u) *dst++ = (int)(p0 + e);
+      off += total;
+    }
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) x[j] = y[j];
+  }
+}
+
+template <class T> bool compact_seg_applies(const CompactJob& job) {
+  return (uintptr_t)job.in % 16 == 0 && job.n * (long long)sizeof(T) <= kSegMaxBytes;
+}
+
 template <class T> size_t compact_temp_bytes(long long n) {
-  return kHeaderBytes + round_up((size_t)rows_tiles<T>(1, n) * 8, 256);
+  const size_t rows = kHeaderBytes + round_up((size_t)rows_tiles<T>(1, n) * 8, 256);
+  const size_t seg = kHeaderBytes + seg_status_bytes<unsigned>();
+  return rows > seg ? rows : seg;
+}
+
+template <class T> cudaError_t launch_compact_seg(const CompactJob& job, const LaunchCtx& ctx, unsigned predmask) {
+  using G = SegGeom<T>;
+  const SegPlan p = seg_plan<G>(job.n, ctx.num_sms);
+  if (p.ctas == 0) return cudaSuccess;
+  CompactSegArgs<T> a;
+  a.n = job.n;
+  a.nc = p.nc;
+  a.warps = p.warps;
+  a.ctas = p.ctas;
+  a.counter = (unsigned*)job.temp;
+  a.err = ctx.err;
+  a.wait_ns = ctx.wait_ns;
+  a.stalled = ctx.stalled_tile;
+  a.in = (const T*)job.in;
+  memcpy(&a.thr, job.threshold_host, sizeof(T));
+  a.predmask = predmask;
+  a.out_idx = job.out_idx;
+  a.out_count = job.out_count;
+  PackedStatus<unsigned> st = seg_status<unsigned>(job.temp);
+  cudaError_t e = cudaMemsetAsync(job.temp, 0, seg_reset_bytes<unsigned>(), ctx.stream);
+  if (e != cudaSuccess) return e;
+  profile_before(ctx);
+  compact_seg_kernel<T, G><<<p.ctas, G::NT, 0, ctx.stream>>>(a, st);
+  profile_after(ctx);
+  return cudaGetLastError();
 }
 
 template <class T> cudaError_t launch_compact(const CompactJob& job, const LaunchCtx& ctx) {
   using G = RowsGeom<T>;
+  static const unsigned masks[6] = {1u, 3u, 4u, 6u, 2u, 13u};  // LT LE GT GE EQ NE
+  if (compact_seg_applies<T>(job)) return launch_compact_seg<T>(job, ctx, masks[job.pred]);
   CompactArgs<T> a;
   a.in = (const T*)job.in;
   a.n = job.n;
   a.num_tiles = rows_tiles<T>(1, job.n);
   memcpy(&a.thr, job.threshold_host, sizeof(T));
-  static const unsigned masks[6] = {1u, 3u, 4u, 6u, 2u, 13u};  // LT LE GT GE EQ NE
   a.predmask = masks[job.pred];
   a.out_idx = job.out_idx;
   a.out_count = job.out_count;
@@ -170,7 +317,7 @@ template <class T> cudaError_t launch_compact(const CompactJob& job, const Launc
   a.stalled_tile = ctx.stalled_tile;
   PackedStatus<unsigned> st;
   st.w = (unsigned long long*)((char*)job.temp + kHeaderBytes);
-  cudaError_t e = cudaMemsetAsync(job.temp, 0, compact_temp_bytes<T>(job.n), ctx.stream);
+  cudaError_t e = cudaMemsetAsync(job.temp, 0, kHeaderBytes + round_up((size_t)a.num_tiles * 8, 256), ctx.stream);
   if (e != cudaSuccess) return e;
   profile_before(ctx);
   compact_kernel<T><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);

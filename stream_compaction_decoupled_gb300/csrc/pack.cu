@@ -32,8 +32,8 @@ struct PackArgs {
   long long stalled_tile;
 };
 
-__global__ void __launch_bounds__(RowsGeom<unsigned>::NT, RowsGeom<unsigned>::MINB) pack_kernel(PackArgs a, PackedStatus<unsigned> st) {
-  using G = RowsGeom<unsigned>;
+template <class G>
+__global__ void __launch_bounds__(G::NT, G::MINB) pack_kernel(PackArgs a, PackedStatus<unsigned> st) {
   constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, TILE = G::TILE;
   __shared__ __align__(128) unsigned s_tile[TILE];
   __shared__ __align__(8) unsigned long long s_bar;
@@ -177,16 +177,19 @@ __global__ void __launch_bounds__(RowsGeom<unsigned>::NT, RowsGeom<unsigned>::MI
   }
 }
 
+// Packing geometry: the record emission, not the scan, dominates, so tiles are
+// a quarter of the scans' (1024 counts: four times as many CTAs share the emission).
+using PackGeom = RowsCfg<unsigned, 128, 2, 2, 12>;
+
 size_t pack_temp_bytes(long long n) {
-  return kHeaderBytes + round_up((size_t)rows_tiles<unsigned>(1, n) * 8, 256);
+  return kHeaderBytes + round_up((size_t)rows_tiles<unsigned, PackGeom>(1, n) * 8, 256);
 }
 
-cudaError_t launch_pack(const PackJob& job, const LaunchCtx& ctx) {
-  using G = RowsGeom<unsigned>;
+template <class G> cudaError_t launch_pack_geom(const PackJob& job, const LaunchCtx& ctx) {
   PackArgs a;
   a.counts = job.counts;
   a.n = job.n;
-  a.num_tiles = rows_tiles<unsigned>(1, job.n);
+  a.num_tiles = rows_tiles<unsigned, G>(1, job.n);
   a.offsets = job.offsets;
   a.records = job.records;
   a.capacity = job.capacity;
@@ -199,12 +202,15 @@ cudaError_t launch_pack(const PackJob& job, const LaunchCtx& ctx) {
   a.stalled_tile = ctx.stalled_tile;
   PackedStatus<unsigned> st;
   st.w = (unsigned long long*)((char*)job.temp + kHeaderBytes);
-  cudaError_t e = cudaMemsetAsync(job.temp, 0, pack_temp_bytes(job.n), ctx.stream);
+  cudaError_t e = cudaMemsetAsync(
+      job.temp, 0, kHeaderBytes + round_up((size_t)rows_tiles<unsigned, G>(1, job.n) * 8, 256), ctx.stream);
   if (e != cudaSuccess) return e;
   profile_before(ctx);
-  pack_kernel<<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
+  pack_kernel<G><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
   profile_after(ctx);
   return cudaGetLastError();
 }
+
+cudaError_t launch_pack(const PackJob& job, const LaunchCtx& ctx) { return launch_pack_geom<PackGeom>(job, ctx); }
 
 }  // namespace gbs

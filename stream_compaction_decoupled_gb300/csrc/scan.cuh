@@ -1,10 +1,12 @@
 // scan.cuh -- dispatch of a scan along the middle axis of a row-major (B, R, C)
-// array: C == 1 (contiguous rows) goes to the row kernel, C > 1 (lanes / columns)
-// to the lane kernel.
+// array.  C == 1 (contiguous rows): one row that fits in L2 goes to the segment
+// kernel, one row many times larger than L2 to the L2-resident look-back kernel,
+// everything else to the row kernel.  C > 1 (lanes / columns): the lane kernel.
 #pragma once
 
 #include "scan_lanes.cuh"
 #include "scan_rows.cuh"
+#include "scan_seg.cuh"
 #include "scan_stash.cuh"
 
 namespace gbs {
@@ -14,12 +16,21 @@ template <class T> size_t scan_temp_bytes(long long B, long long R, long long C)
     // Either kernel may run (the choice depends on the pointers' alignment).
     const size_t rows = kHeaderBytes + rows_status_bytes<T>(rows_tiles<T>(B, R));
     const size_t stash = B == 1 ? kHeaderBytes + stash_status_bytes<T>(R) : 0;
-    return rows > stash ? rows : stash;
+    const size_t seg = B == 1 ? kHeaderBytes + seg_status_bytes<T>() : 0;
+    const size_t m = rows > stash ? rows : stash;
+    return m > seg ? m : seg;
   }
   return lanes_temp_bytes<T>(B, R, C);
 }
 
 template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& ctx) {
+  if (seg_applies<T>(job)) {
+    switch (job.op) {
+      case OP_ADD: return launch_seg_op<T, OP_ADD>(job, ctx);
+      case OP_MAX: return launch_seg_op<T, OP_MAX>(job, ctx);
+      default: return launch_seg_op<T, OP_MIN>(job, ctx);
+    }
+  }
   if (job.C == 1 && stash_applies<T>(job, ctx.num_sms)) {
     switch (job.op) {
       case OP_ADD: return launch_stash_op<T, OP_ADD>(job, ctx);

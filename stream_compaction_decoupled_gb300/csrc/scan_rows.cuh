@@ -53,7 +53,12 @@ template <class T, int NT_, int ROUNDS_, int K_, int MINB_> struct RowsCfg {
 // CTAs (tiles) are resident per SM, and a look-back window of 32 x 2 tiles.  (A
 // sweep on the fp32 1e8 scan: windows of 4 or 8 tiles per lane were slower, 6 CTAs
 // of 256 threads were slower, 32 KB tiles were no faster.)
-template <class T> using RowsGeom = RowsCfg<T, 128, 8, 2, 12>;
+// fp64 runs the chunked variant (see scan_rows_chunk_kernel), which keeps a thread's
+// 16 doubles in registers; 8 CTAs per SM (64 registers a thread) let one tile's
+// FP64 adds overlap other tiles' loads and look-backs best (113 us against 130 us
+// at 4 CTAs for 1e7 doubles).
+template <class T>
+using RowsGeom = RowsCfg<T, 128, 8, 2, std::is_same<T, double>::value ? 8 : 12>;
 
 template <class T, int OP, class G, class S>
 __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_kernel(RowsArgs<T> a, S st) {
@@ -363,9 +368,8 @@ cudaError_t launch_rows_op(const ScanJob& job, const LaunchCtx& ctx) {
   if (e != cudaSuccess) return e;
   profile_before(ctx);
   if constexpr (std::is_same<T, double>::value) {
-    // fp64: thread-contiguous chunks (fewer operator applications), fewer CTAs per SM.
-    using GC = RowsCfg<T, G::NT, G::ROUNDS, G::K, 4>;
-    scan_rows_chunk_kernel<T, OP, GC, decltype(st)><<<a.num_tiles, GC::NT, 0, ctx.stream>>>(a, st);
+    // fp64: thread-contiguous chunks (fewer operator applications).
+    scan_rows_chunk_kernel<T, OP, G, decltype(st)><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
   } else {
     scan_rows_kernel<T, OP, G, decltype(st)><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
   }

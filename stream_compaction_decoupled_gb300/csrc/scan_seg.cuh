@@ -1,0 +1,387 @@
+// scan_seg.cuh -- reduce-then-scan in one launch, for 1-D inputs that fit in L2.
+//
+// The CUDA Handbook, 13.3.3 (Figure 13-10) splits the input into subarrays, reduces
+// each (pass 1), scans the partial sums, and rescans each subarray seeded with its
+// base sum (pass 2): 3N global operations over three launches.  Here the three
+// steps run in one kernel and the second read of every element is served from L2,
+// so HBM sees one read and one write per element, as a single-pass scan does:
+//
+//   1. each CTA claims a segment (an atomic counter: a CTA only ever waits for
+//      segments claimed before its own, so no co-residency is assumed) and its
+//      warps reduce their contiguous parts of it, loading with an L2 evict-last
+//      hint; the block combines the warp totals and publishes the segment
+//      aggregate;
+//   2. warp 0 reads the aggregates of ALL earlier segments at once (lane l owns
+//      segments l, l+32, ...) and combines them in a fixed order: the segment's
+//      base sum.  There is no chain of inclusive prefixes to walk, so every
+//      segment has its base one memory round trip after the slowest earlier
+//      segment has published, however many segments there are;
+//   3. each warp rescans its part chunk by chunk from L2 (evict-first: last use),
+//      seeded with base sum (+) earlier warps of the segment (+) earlier chunks,
+//      and streams the result out.
+//
+// Decoupled look-back (The CUDA Handbook, 13.3.4) is the better scheme once the
+// input is many times larger than L2 and tiles start at different times; with all
+// tiles of a mid-size input starting together, the look-back's inclusive prefixes
+// can only advance one window of tiles per memory round trip, which this kernel
+// avoids.  The fixed combination order makes floating-point results reproducible
+// from run to run.
+//
+// Stream compaction (B. Merry, "Prefix sums on GPUs", slide "Solution") runs the
+// same three phases on selection counts.
+#pragma once
+
+#include "launch.h"
+#include "tile.cuh"
+
+namespace gbs {
+
+// A warp's unit of work is a chunk of 32 lanes x ROUNDS x one 16-byte vector; in
+// round j lane l holds vector j*32 + l of the chunk (the row kernel's run layout).
+template <class T, int NT_, int ROUNDS_, int MINB_> struct SegCfg {
+  static constexpr int NT = NT_, NW = NT_ / 32, ROUNDS = ROUNDS_, MINB = MINB_;
+  static constexpr int VEC = Vec<T>::N;
+  static constexpr int CH = 32 * ROUNDS * VEC;  // elements per chunk
+  static constexpr int MAXSEG = 512;            // segments (CTAs) per launch at most
+  static constexpr int M = MAXSEG / 32;         // earlier aggregates per lane in phase 2
+};
+template <class T> using SegGeom = SegCfg<T, 1024, 4, 1>;
+
+// Work split: nc chunks over `warps` warps (warp w of the grid takes chunks
+// [w*nc/warps, (w+1)*nc/warps), at least one each), NW warps per CTA.
+struct SegPlan {
+  long long nc = 0;
+  unsigned warps = 0;
+  unsigned ctas = 0;
+};
+template <class G> SegPlan seg_plan(long long n, int num_sms) {
+  SegPlan p;
+  p.nc = (n + G::CH - 1) / G::CH;
+  long long w = (long long)num_sms * G::MINB * G::NW;
+  if (w > (long long)G::MAXSEG * G::NW) w = (long long)G::MAXSEG * G::NW;
+  if (w > p.nc) w = p.nc;
+  p.warps = (unsigned)w;
+  p.ctas = (unsigned)((w + G::NW - 1) / G::NW);
+  return p;
+}
+
+struct SegArgsBase {
+  long long n;
+  long long nc;
+  unsigned warps;
+  unsigned ctas;
+  unsigned* counter;
+  unsigned* err;
+  unsigned long long wait_ns;
+  long long stalled;  // fault injection: this segment never publishes
+};
+
+template <class T> struct SegArgs : SegArgsBase {
+  const T* in;
+  T* out;
+  T init;
+  int inclusive;
+};
+
+// Chunk loads and stores.  A full chunk moves as 16-byte vectors with an L2 policy;
+// the one ragged chunk at the end of the input moves element by element (elements
+// past n read as T{}: they only ever reach totals that nothing reads).
+template <class T, int ROUNDS>
+__device__ __forceinline__ void seg_load(Vec<T> (&x)[ROUNDS], const T* in, long long c0, long long n, int lane,
+                                         unsigned long long pol) {
+  constexpr int VEC = Vec<T>::N, CH = 32 * ROUNDS * VEC;
+  if (c0 + CH <= n) {
+    const uint4* p = reinterpret_cast<const uint4*>(in + c0) + lane;
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+      const uint4 u = ld_hint(p + j * 32, pol);
+      memcpy(x[j].v, &u, 16);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const long long i = c0 + (long long)(j * 32 + lane) * VEC + e;
+        x[j].v[e] = i < n ? in[i] : T{};
+      }
+  }
+}
+template <class T, int ROUNDS>
+__device__ __forceinline__ void seg_store(const Vec<T> (&x)[ROUNDS], T* out, long long c0, long long n, int lane,
+                                          unsigned long long pol) {
+  constexpr int VEC = Vec<T>::N, CH = 32 * ROUNDS * VEC;
+  if (c0 + CH <= n) {
+    uint4* p = reinterpret_cast<uint4*>(out + c0) + lane;
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+      uint4 u;
+      memcpy(&u, x[j].v, 16);
+      st_hint(p + j * 32, u, pol);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const long long i = c0 + (long long)(j * 32 + lane) * VEC + e;
+        if (i < n) out[i] = x[j].v[e];
+      }
+  }
+}
+
+// Butterfly combination over the warp (every lane gets the same result; the order
+// is fixed, so floating-point sums are reproducible).
+template <class T, int OP> __device__ __forceinline__ T warp_allreduce(T v) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const T o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = (threadIdx.x & off) ? Op<T, OP>::f(o, v) : Op<T, OP>::f(v, o);
+  }
+  return v;
+}
+
+// Phase 1 of a warp: the combination of the elements of its chunks [c0, c1), read
+// as coalesced 16-byte vectors, U per lane in flight (the reduction's order is free:
+// only the scan in phase 3 follows element order).  Loads carry the L2 evict-last
+// hint so that phase 3 finds the lines in L2.  Every lane of a warp with whole
+// chunks has elements; only the last warp (whose total nothing reads) may not.
+template <class T, int OP, class G>
+__device__ __forceinline__ T seg_reduce_part(const T* in, long long n, long long c0, long long c1, int lane) {
+  constexpr int VEC = G::VEC, CH = G::CH, U = 8;
+  const unsigned long long keep = l2_policy_evict_last();
+  const long long e1 = c1 * CH < n ? c1 * CH : n;
+  const long long v1 = e1 / VEC;  // whole vectors end
+  const uint4* p = reinterpret_cast<const uint4*>(in);
+  long long v = c0 * CH / VEC + lane;
+  T acc{};
+  if (v < v1) {
+    const uint4 u = ld_hint(p + v, keep);
+    Vec<T> x;
+    memcpy(x.v, &u, 16);
+    acc = x.v[0];
+#pragma unroll
+    for (int e = 1; e < VEC; ++e) acc = Op<T, OP>::f(acc, x.v[e]);
+    v += 32;
+  }
+  for (; v + 32 * (U - 1) < v1; v += 32 * U) {
+    uint4 u[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      Vec<T> x;
+      memcpy(x.v, &u[k], 16);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc = Op<T, OP>::f(acc, x.v[e]);
+    }
+  }
+  for (; v < v1; v += 32) {
+    const uint4 u = ld_hint(p + v, keep);
+    Vec<T> x;
+    memcpy(x.v, &u, 16);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc = Op<T, OP>::f(acc, x.v[e]);
+  }
+  if (lane == 0)
+    for (long long i = v1 * VEC; i < e1; ++i) acc = Op<T, OP>::f(acc, in[i]);
+  return acc;
+}
+
+// Phase 2, by one whole warp: the combination of the aggregates of segments
+// 0..seg-1 (seg >= 1), waiting (bounded by wait_ns) for each to be published.
+// Lane l owns segments l, l+32, ...: all are requested at once, and only those not
+// yet published are read again.  Returns the base sum in every lane.
+template <class T, int OP, int M, class S>
+__device__ __forceinline__ T seg_gather(const S& st, unsigned seg, unsigned long long wait_ns, bool& timed_out) {
+  const int lane = threadIdx.x & 31;
+  T val[M];
+  unsigned pending = 0;
+#pragma unroll
+  for (int k = 0; k < M; ++k)
+    if ((unsigned)(lane + 32 * k) < seg) pending |= 1u << k;
+  unsigned long long t0 = 0;
+  timed_out = false;
+  for (int spins = 0;; ++spins) {
+#pragma unroll
+    for (int k = 0; k < M; ++k) {
+      if (pending & (1u << k)) {
+        T v;
+        const unsigned f = st.poll(lane + 32 * k, v);
+        if (f != FLAG_X) {
+          val[k] = st.fetch(lane + 32 * k, f, v);
+          pending &= ~(1u << k);
+        }
+      }
+    }
+    if (__all_sync(0xffffffffu, pending == 0)) break;
+    unsigned long long now = 0;
+    if (lane == 0) now = globaltimer();
+    now = __shfl_sync(0xffffffffu, now, 0);
+    if (spins == 0) t0 = now;
+    else if (now - t0 > wait_ns) {
+      timed_out = true;
+#pragma unroll
+      for (int k = 0; k < M; ++k)
+        if (pending & (1u << k)) val[k] = T{};
+      break;
+    }
+    backoff(spins);
+  }
+  // Lane fold in segment order, then the lanes in lane order.  A lane with no
+  // segment contributes the identity of add, or (max / min being idempotent) lane
+  // 0's first value.
+  T acc = val[0];
+#pragma unroll
+  for (int k = 1; k < M; ++k)
+    if ((unsigned)(lane + 32 * k) < seg) acc = Op<T, OP>::f(acc, val[k]);
+  const T first = __shfl_sync(0xffffffffu, val[0], 0);
+  if ((unsigned)lane >= seg) acc = OP == OP_ADD ? T{} : first;
+  const T inc = warp_inclusive<T, OP>(acc, lane);
+  return __shfl_sync(0xffffffffu, inc, 31);
+}
+
+// The segment's share of the chunks for warp `warp` of the CTA.
+__device__ __forceinline__ void seg_chunks(const SegArgsBase& a, unsigned seg, int warp, int nw, long long& c0,
+                                           long long& c1) {
+  const long long w = (long long)seg * nw + warp;
+  c0 = c1 = 0;
+  if (w < (long long)a.warps) {
+    c0 = w * a.nc / a.warps;
+    c1 = (w + 1) * a.nc / a.warps;
+  }
+}
+
+template <class T, int OP, class G, class S>
+__global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, S st) {
+  constexpr int NW = G::NW, ROUNDS = G::ROUNDS, CH = G::CH;
+  __shared__ unsigned s_seg;
+  __shared__ T s_warp[NW];
+  __shared__ T s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
+  __syncthreads();
+  const unsigned seg = s_seg;
+  long long c0, c1;
+  seg_chunks(a, seg, warp, NW, c0, c1);
+
+  // Phase 1: the warp's total (lanes accumulate their vectors, then one butterfly).
+  const T acc = seg_reduce_part<T, OP, G>(a.in, a.n, c0, c1, lane);
+  const T wtot = warp_allreduce<T, OP>(acc);
+  if (lane == 0) s_warp[warp] = wtot;  // a warp without chunks exists only at the end of the last segment
+  __syncthreads();
+
+  // Phase 2: publish the segment aggregate, gather the earlier ones.
+  if (warp == 0) {
+    const T agg = block_scan_warp_totals<T, OP, NW>(s_warp, lane);
+    if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
+    if (seg > 0) {
+      bool timed_out;
+      const T base = seg_gather<T, OP, G::M>(st, seg, a.wait_ns, timed_out);
+      if (lane == 0) {
+        s_base = base;
+        if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+      }
+    }
+  }
+  __syncthreads();
+
+  // Phase 3: rescan the warp's chunks from L2, seeded.
+  bool hb = seg > 0;
+  T base = s_base;
+  if (warp > 0) {
+    const T wp = s_warp[warp - 1];
+    base = hb ? Op<T, OP>::f(base, wp) : wp;
+    hb = true;
+  }
+  if (!a.inclusive) {
+    base = hb ? Op<T, OP>::f(a.init, base) : a.init;
+    hb = true;
+  }
+  const unsigned long long drop = l2_policy_evict_first();
+  Vec<T> x[ROUNDS];
+  if (c0 < c1) seg_load<T, ROUNDS>(x, a.in, c0 * CH, a.n, lane, drop);
+  for (long long c = c0; c < c1; ++c) {
+    Vec<T> y[ROUNDS];  // the next chunk, requested before this one is scanned
+    if (c + 1 < c1) seg_load<T, ROUNDS>(y, a.in, (c + 1) * CH, a.n, lane, drop);
+    T pre[ROUNDS];
+    const T ctot = regs_reduce_pass<T, OP, ROUNDS>(x, lane, pre);
+    regs_apply_pass<T, OP, ROUNDS>(x, lane, pre, base, hb, a.inclusive);
+    seg_store<T, ROUNDS>(x, a.out, c * CH, a.n, lane, drop);
+    base = hb ? Op<T, OP>::f(base, ctot) : ctot;
+    hb = true;
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) x[j] = y[j];
+  }
+}
+
+// Status area: MAXSEG descriptors right after the header.
+template <class T> size_t seg_status_bytes() {
+  using G = SegGeom<T>;
+  if (sizeof(T) == 4) return round_up((size_t)G::MAXSEG * 8, 256);
+  return round_up((size_t)G::MAXSEG * 4, 256) + 2 * round_up((size_t)G::MAXSEG * sizeof(T), 256);
+}
+template <class T> typename StatusFor<T>::type seg_status(void* temp) {
+  using G = SegGeom<T>;
+  typename StatusFor<T>::type st;
+  char* base = (char*)temp + kHeaderBytes;
+  if constexpr (sizeof(T) == 4) {
+    st.w = (unsigned long long*)base;
+  } else {
+    st.flag = (unsigned*)base;
+    base += round_up((size_t)G::MAXSEG * 4, 256);
+    st.agg = (T*)base;
+    base += round_up((size_t)G::MAXSEG * sizeof(T), 256);
+    st.pfx = (T*)base;
+  }
+  return st;
+}
+// Bytes to clear before a launch: the header and the flags.
+template <class T> size_t seg_reset_bytes() {
+  using G = SegGeom<T>;
+  return kHeaderBytes + (sizeof(T) == 4 ? (size_t)G::MAXSEG * 8 : (size_t)G::MAXSEG * 4);
+}
+
+// Inputs up to this size go to this kernel.  Measured on GB300 (fp32 add, L2
+// flushed): 12.3 / 24.6 / 32.8 us at 1e6 / 1e7 / 1.6e7 elements against 17.4 /
+// 33.0 / 45.1 us for the row kernel and 30.7 / 38.9 us for the L2-resident
+// look-back kernel at 1e7 / 1.6e7; at 3.2e7 (128 MB) the two meet.
+constexpr long long kSegMaxBytes = 96ll << 20;
+
+// Not for fp64: this kernel's run layout costs about five fp64 adds per element
+// (warp scans of 2-element vectors), the row kernel's thread-contiguous chunks
+// about 2.4, and fp64 adds, not bytes, bound fp64 scans on GB300.
+template <class T> bool seg_applies(const ScanJob& job) {
+  if (std::is_same<T, double>::value) return false;
+  return job.B == 1 && job.C == 1 && (uintptr_t)job.in % 16 == 0 && (uintptr_t)job.out % 16 == 0 &&
+         job.R * (long long)sizeof(T) <= kSegMaxBytes;
+}
+
+template <class T, int OP, class G = SegGeom<T>>
+cudaError_t launch_seg_op(const ScanJob& job, const LaunchCtx& ctx) {
+  const SegPlan p = seg_plan<G>(job.R, ctx.num_sms);
+  if (p.ctas == 0) return cudaSuccess;
+  SegArgs<T> a;
+  a.n = job.R;
+  a.nc = p.nc;
+  a.warps = p.warps;
+  a.ctas = p.ctas;
+  a.counter = (unsigned*)job.temp;
+  a.err = ctx.err;
+  a.wait_ns = ctx.wait_ns;
+  a.stalled = ctx.stalled_tile;
+  a.in = (const T*)job.in;
+  a.out = (T*)job.out;
+  a.init = T{};
+  if (!job.inclusive && job.init_host) memcpy(&a.init, job.init_host, sizeof(T));
+  a.inclusive = job.inclusive;
+  auto st = seg_status<T>(job.temp);
+  cudaError_t e = cudaMemsetAsync(job.temp, 0, seg_reset_bytes<T>(), ctx.stream);
+  if (e != cudaSuccess) return e;
+  profile_before(ctx);
+  scan_seg_kernel<T, OP, G, decltype(st)><<<p.ctas, G::NT, 0, ctx.stream>>>(a, st);
+  profile_after(ctx);
+  return cudaGetLastError();
+}
+
+}  // namespace gbs

@@ -54,13 +54,38 @@ def test_compact_none_all_and_empty():
     assert int(cnt.item()) == 0
 
 
-def test_compact_unaligned():
-    x = workloads.uniform01(5 * 4096 + 3, np.float32, 8)
+@pytest.mark.parametrize("dt", [np.float32, np.float64, np.int32])
+@pytest.mark.parametrize("n", [2, 4097, 5 * 4096 + 3, 1_000_003])
+@pytest.mark.parametrize("pred", ["lt", "ne"])
+def test_compact_unaligned(dt, n, pred):
+    """An input that is not 16-byte aligned takes the tile kernel (decoupled look-back)."""
+    if np.dtype(dt).kind == "f":
+        x = workloads.uniform01(n + 1, dt, n + 8)
+        thr = 0.3
+    else:
+        x = workloads.small_ints(n + 1, n + 8, -10, 10, dtype=dt)
+        thr = 0
     xd = dev(x)[1:]
-    idx, cnt = gb.compact(xd, "lt", 0.3)
-    want = oracle.compact(x[1:], "lt", 0.3)
+    idx, cnt = gb.compact(xd, pred, thr)
+    want = oracle.compact(x[1:], pred, thr)
     c = int(cnt.item())
     assert c == want.size and np.array_equal(idx[:c].cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("n", [511, 512, 513, 16_384 + 5, 2_490_368, 2_490_368 + 1, 25_165_824])
+def test_compact_segment_sizes(n):
+    """Chunk, CTA and warp-saturation boundaries of the segment kernel, up to 96 MiB."""
+    x = workloads.uniform01(n, np.float32, n % 977)
+    check_compact(x, "lt", 0.5, "seg n=%d" % n)
+    check_compact(x, "ge", 0.999, "seg sparse n=%d" % n)
+    assert gb.device_error() == gb.OK
+
+
+def test_compact_above_segment_limit():
+    """Above 96 MiB the tile kernel runs even for aligned inputs."""
+    x = workloads.uniform01(26_000_003, np.float32, 11)
+    check_compact(x, "lt", 0.25, "tile kernel n=26e6")
+    assert gb.device_error() == gb.OK
 
 
 def test_compact_nan():

@@ -57,22 +57,27 @@ def stall():
     gb.set_wait_limit_ns(0)
 
 
-@pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "compact", "pack", "l2_resident"])
+@pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "segments", "compact_segments",
+                                  "compact_tiles", "pack", "l2_resident"])
 def test_stalled_tile_times_out(stall, kind):
-    n = 64 * 4096 if kind != "l2_resident" else 12_000_000
+    n = 64 * 4096 if kind != "l2_resident" else 26_000_000
     x = workloads.uniform01(n, np.float32, 1)
     gb.set_wait_limit_ns(5_000_000)   # 5 ms
     gb.set_stalled_tile(3)
-    if kind == "rows_f32":
-        gb.scan_inclusive(dev(x))
+    if kind == "rows_f32":  # an unaligned view: the row kernel
+        gb.scan_inclusive(dev(np.concatenate([x[:1], x]))[1:])
     elif kind == "rows_f64":
         gb.scan_inclusive(dev(x.astype(np.float64)))
     elif kind == "lanes":
         gb.scan_inclusive(dev(x), lanes=8)
+    elif kind == "segments":  # 512 chunks -> 16 segments; segment 3 never publishes
+        gb.scan_inclusive(dev(x))
     elif kind == "l2_resident":  # one long row: the stalled index is a run of 4 tiles
         gb.scan_inclusive(dev(x))
-    elif kind == "compact":
+    elif kind == "compact_segments":
         gb.compact(dev(x), "lt", 0.5)
+    elif kind == "compact_tiles":
+        gb.compact(dev(np.concatenate([x[:1], x]))[1:], "lt", 0.5)
     else:
         gb.pack_by_counts(dev((x * 8).astype(np.int32)), 8 * n)
     assert gb.device_error() == gb.ERR_TIMEOUT

@@ -178,13 +178,63 @@ def test_full_size_workload(name):
     assert gb.device_error() == gb.OK
 
 
-# ---- the L2-resident single-pass path (one long aligned row) ----------------------
-# It applies from 152 SMs x 4 tiles x 4 runs upwards: 9,961,472 four-byte or
-# 4,980,736 eight-byte elements.
+# ---- the segment kernel (one aligned row of at most 96 MiB) ------------------------
+# A warp's chunk holds 512 four-byte or 256 eight-byte elements; 152 SMs x 32 warps
+# saturate at 4864 chunks (2,490,368 / 1,245,184 elements), beyond which warps take
+# several chunks.  fp64 stays on the row kernel.
 
-@pytest.mark.parametrize("dt,n", [("f32", 9_961_472), ("f32", 9_961_472 + 77), ("f32", 33_554_432 + 5),
-                                  ("i32", 12_000_001), ("u32", 10_000_000), ("f64", 4_980_736 + 1),
-                                  ("i64", 7_000_003), ("f64", 16_777_216)])
+SEG_SMALL = [1, 511, 512, 513, 16_384 + 5, 2 * 16_384 + 1, 2_490_368, 2_490_368 + 1, 3_000_017]
+
+
+@pytest.mark.parametrize("dt", ["i32", "u32", "f32", "i64", "u64"])
+@pytest.mark.parametrize("op", ["add", "max", "min"])
+@pytest.mark.parametrize("n", SEG_SMALL)
+def test_segment_path(dt, op, n):
+    if dt not in DTYPES:
+        pytest.skip("no torch dtype")
+    x = make(dt, n, 7 + n % 1000)
+    xd = to_dev(x)
+    got = to_host(gb.scan_inclusive(xd, op))
+    assert_scan_matches(got, as3(x, 1, n, 1), op, True, what="seg %s %s incl n=%d" % (dt, op, n))
+    init = x[0] if op != "add" else None
+    got = to_host(gb.scan_exclusive(xd, op, init=init))
+    assert_scan_matches(got, as3(x, 1, n, 1), op, False, init, what="seg %s %s excl n=%d" % (dt, op, n))
+    assert gb.device_error() == gb.OK
+
+
+@pytest.mark.parametrize("dt,n", [("f32", 10_000_019), ("i32", 25_165_824), ("f32", 25_165_824),
+                                  ("u64", 12_582_912), ("i64", 7_000_003)])
+def test_segment_path_large(dt, n):
+    """Up to the 96 MiB limit, where every warp takes several chunks."""
+    if dt not in DTYPES:
+        pytest.skip("no torch dtype")
+    x = make(dt, n, n % 1000)
+    xd = to_dev(x)
+    for op in ("add", "max"):
+        got = to_host(gb.scan_inclusive(xd, op))
+        assert_scan_matches(got, as3(x, 1, n, 1), op, True, what="seg %s %s n=%d" % (dt, op, n))
+    got = to_host(gb.scan_exclusive(xd, "add"))
+    assert_scan_matches(got, as3(x, 1, n, 1), "add", False, what="seg %s excl n=%d" % (dt, n))
+    assert gb.device_error() == gb.OK
+
+
+def test_segment_path_reproducible_and_in_place():
+    """The segment kernel combines in a fixed order: fp32 sums repeat bit for bit."""
+    x = workloads.normal(10_000_000, np.float32, 21)
+    xd = to_dev(x)
+    first = to_host(gb.scan_inclusive(xd))
+    for _ in range(3):
+        assert np.array_equal(to_host(gb.scan_inclusive(xd)), first)
+    y = to_dev(x)
+    gb.scan_inclusive(y, out=y)
+    assert np.array_equal(to_host(y), first)
+    assert gb.device_error() == gb.OK
+
+
+# ---- the L2-resident single-pass path (one long aligned row above 96 MiB) ------------
+
+@pytest.mark.parametrize("dt,n", [("f32", 25_165_824 + 77), ("f32", 33_554_432 + 5), ("i32", 30_000_001),
+                                  ("u32", 26_000_000), ("i64", 13_000_003), ("u64", 12_582_912 + 8)])
 @pytest.mark.parametrize("op", ["add", "max", "min"])
 def test_l2_resident_path(dt, n, op):
     if dt not in DTYPES:
@@ -200,10 +250,24 @@ def test_l2_resident_path(dt, n, op):
 
 
 def test_l2_resident_path_repeated_in_place():
-    x = workloads.small_ints(20_000_000, 5, -3, 4)
+    x = workloads.small_ints(30_000_000, 5, -3, 4)
     want = oracle.scan(x)
     for _ in range(5):
         y = to_dev(x)
         gb.scan_inclusive(y, out=y)
         assert np.array_equal(to_host(y), want)
+    assert gb.device_error() == gb.OK
+
+
+# ---- the row kernel on one row (unaligned views never take the other kernels) ---------
+
+@pytest.mark.parametrize("dt", ["i32", "f32", "f64", "i64"])
+@pytest.mark.parametrize("n", [4097, 1_000_003, 10_000_001])
+def test_row_kernel_single_row(dt, n):
+    base = make(dt, n + 1, 3 + n % 100)
+    xd = to_dev(base)[1:]
+    got = to_host(gb.scan_inclusive(xd))
+    assert_scan_matches(got, as3(base[1:], 1, n, 1), "add", True, what="rows %s n=%d" % (dt, n))
+    got = to_host(gb.scan_inclusive(xd, "min"))
+    assert_scan_matches(got, as3(base[1:], 1, n, 1), "min", True, what="rows %s min n=%d" % (dt, n))
     assert gb.device_error() == gb.OK
