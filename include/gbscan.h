@@ -20,7 +20,15 @@
  *     `threshold` are HOST pointers to one element, read during the call.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Every call is asynchronous on that stream; nothing synchronises
- *     unless stated.
+ *     unless stated.  A call enqueues a small status-clearing kernel and its main
+ *     kernel(s), each launched with programmatic stream serialization (programmatic
+ *     dependent launch): each may be scheduled while the grid before it in the
+ *     stream still runs, and each waits (griddepcontrol.wait) for that grid to
+ *     complete before touching memory, so stream order is kept.  The library's
+ *     kernels let the next launch in the stream be scheduled early; a caller's
+ *     kernel launched after a call with the same attribute must itself execute
+ *     griddepcontrol.wait (cudaGridDependencySynchronize) before reading the
+ *     call's outputs, as that attribute requires of any kernel.
  *   - An "element" is `lanes` consecutive values of `dtype` (lanes = 1 for plain
  *     arrays; 24 fp32 lanes for a 96-byte struct; 17 fp64 lanes for a dual number
  *     with 16 partials).  Operators act lane-wise.
@@ -205,10 +213,11 @@ int gb_version(void);
 
 /*
  * Observability hook: when both are non-NULL cudaEvent_t handles, the next calls
- * on this host thread record `before` and `after` on their stream immediately
- * around their main kernel launch (the single-pass kernel, or the last of the
- * reduce-then-scan launches), so a caller can time that kernel alone.  Pass
- * NULL, NULL to turn it off.
+ * on this host thread record `before` and `after` on their stream around their
+ * launches (the status clear and the single-pass kernel, or the three
+ * reduce-then-scan launches), so a caller can time a call's device work without
+ * host overhead.  Nothing is recorded between the launches of a call: an event
+ * there would stop them from overlapping.  Pass NULL, NULL to turn it off.
  */
 void gb_set_profile_events(void* before, void* after);
 

@@ -14,6 +14,29 @@
 // negative counts), one word per device, set with atomicOr by the kernels.
 __device__ unsigned g_gbscan_device_error;
 
+namespace gbs {
+
+// The status clear (see clear_status in launch.h): 16-byte stores over both ranges.
+__global__ void __launch_bounds__(256) clear_status_kernel(uint4* p0, size_t n0, uint4* p1, size_t n1) {
+  pdl_entry();
+  const size_t n = n0 + n1;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    if (i < n0) p0[i] = make_uint4(0u, 0u, 0u, 0u);
+    else p1[i - n0] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+cudaError_t clear_status(void* p0, size_t b0, void* p1, size_t b1, const LaunchCtx& ctx) {
+  const size_t n0 = (b0 + 15) / 16, n1 = p1 ? (b1 + 15) / 16 : 0;
+  size_t grid = (n0 + n1 + 1023) / 1024;  // about four stores a thread
+  const size_t max_grid = 2 * (size_t)(ctx.num_sms > 0 ? ctx.num_sms : 1);
+  if (grid > max_grid) grid = max_grid;
+  if (grid < 1) grid = 1;
+  return launch_pdl(clear_status_kernel, (unsigned)grid, 256, 0, ctx.stream, (uint4*)p0, n0, (uint4*)p1, n1);
+}
+
+}  // namespace gbs
+
 namespace {
 
 using gbs::LaunchCtx;

@@ -247,6 +247,21 @@ __device__ __forceinline__ bool aligned16(const void* p) {
   return ((uintptr_t)p & 15u) == 0;
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+
+// Every kernel of the library is launched with programmatic stream serialization
+// (launch_pdl) and begins with pdl_entry(): griddepcontrol.wait returns once the
+// previous grid in the stream has completed and its writes are visible, so inputs
+// written by a preceding kernel, and scratch still in use by a preceding call, are
+// safe to touch after it; griddepcontrol.launch_dependents then lets the next launch
+// in the stream be scheduled while this grid runs (it, too, waits before it reads).
+// The launches of a call thus overlap the kernels before them instead of following
+// them.  Neither instruction spins in software: the wait is a hardware dependency.
+__device__ __forceinline__ void pdl_entry() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- warp scan -------------------------------------------------------------------
 
 // Register-only inclusive warp scan: five __shfl_up_sync doubling steps, each add

@@ -43,6 +43,7 @@ template <class T> __device__ __forceinline__ bool selects(T x, T t, unsigned ma
 
 template <class T>
 __global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_kernel(CompactArgs<T> a, PackedStatus<unsigned> st) {
+  pdl_entry();
   using G = RowsGeom<T>;
   constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, TILE = G::TILE;
   static_assert(ROUNDS * VEC <= 32, "selection bits must fit one word");
@@ -165,6 +166,7 @@ template <class T> struct CompactSegArgs : SegArgsBase {
 
 template <class T, class G>
 __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegArgs<T> a, PackedStatus<unsigned> st) {
+  pdl_entry();
   constexpr int NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, CH = G::CH;
   __shared__ unsigned s_seg;
   __shared__ unsigned s_warp[NW];
@@ -290,12 +292,11 @@ template <class T> cudaError_t launch_compact_seg(const CompactJob& job, const L
   a.out_idx = job.out_idx;
   a.out_count = job.out_count;
   PackedStatus<unsigned> st = seg_status<unsigned>(job.temp);
-  cudaError_t e = cudaMemsetAsync(job.temp, 0, seg_reset_bytes<unsigned>(), ctx.stream);
-  if (e != cudaSuccess) return e;
   profile_before(ctx);
-  compact_seg_kernel<T, G><<<p.ctas, G::NT, 0, ctx.stream>>>(a, st);
+  cudaError_t e = clear_status(job.temp, seg_reset_bytes<unsigned>(), nullptr, 0, ctx);
+  if (e == cudaSuccess) e = launch_pdl(compact_seg_kernel<T, G>, p.ctas, G::NT, 0, ctx.stream, a, st);
   profile_after(ctx);
-  return cudaGetLastError();
+  return e;
 }
 
 template <class T> cudaError_t launch_compact(const CompactJob& job, const LaunchCtx& ctx) {
@@ -317,12 +318,11 @@ template <class T> cudaError_t launch_compact(const CompactJob& job, const Launc
   a.stalled_tile = ctx.stalled_tile;
   PackedStatus<unsigned> st;
   st.w = (unsigned long long*)((char*)job.temp + kHeaderBytes);
-  cudaError_t e = cudaMemsetAsync(job.temp, 0, kHeaderBytes + round_up((size_t)a.num_tiles * 8, 256), ctx.stream);
-  if (e != cudaSuccess) return e;
   profile_before(ctx);
-  compact_kernel<T><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
+  cudaError_t e = clear_status(job.temp, kHeaderBytes + (size_t)a.num_tiles * 8, nullptr, 0, ctx);
+  if (e == cudaSuccess) e = launch_pdl(compact_kernel<T>, a.num_tiles, G::NT, 0, ctx.stream, a, st);
   profile_after(ctx);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace gbs

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace gbs {
 
 // Settings the C ABI attaches to every launch.
@@ -72,7 +74,35 @@ template <class T> cudaError_t launch_rts(const RtsJob& job, const LaunchCtx& ct
 size_t pack_temp_bytes(long long n);
 cudaError_t launch_pack(const PackJob& job, const LaunchCtx& ctx);
 
-// Records ctx.ev_before / ctx.ev_after around the main launch when both are set.
+// Launches `kernel` with programmatic stream serialization, so that it may be
+// scheduled while the previous grid in the stream still runs; the kernel must begin
+// with pdl_entry() (common.cuh), which holds it until that grid has completed.
+template <class... P, class... A>
+cudaError_t launch_pdl(void (*kernel)(P...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
+// Zeroes [p0, p0 + b0) and, if p1 is set, [p1, p1 + b1) with one small kernel
+// launched like the others (it waits for the previous grid, so a call never clears
+// scratch that the call before it still reads).  Both bases 16-byte aligned; the
+// sizes are rounded up to 16 bytes, which the 256-byte-rounded scratch regions hold.
+// Defined in api.cu.
+cudaError_t clear_status(void* p0, size_t b0, void* p1, size_t b1, const LaunchCtx& ctx);
+
+// Records ctx.ev_before / ctx.ev_after around a call's launches (the status clear
+// and the main kernel) when both are set.  Nothing is recorded between the two
+// launches: an event there would stop the second from overlapping the first.
 inline void profile_before(const LaunchCtx& ctx) {
   if (ctx.ev_before && ctx.ev_after) cudaEventRecord(ctx.ev_before, ctx.stream);
 }

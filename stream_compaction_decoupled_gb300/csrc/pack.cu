@@ -34,6 +34,7 @@ struct PackArgs {
 
 template <class G>
 __global__ void __launch_bounds__(G::NT, G::MINB) pack_kernel(PackArgs a, PackedStatus<unsigned> st) {
+  pdl_entry();
   constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, TILE = G::TILE;
   __shared__ __align__(128) unsigned s_tile[TILE];
   __shared__ __align__(8) unsigned long long s_bar;
@@ -202,13 +203,11 @@ template <class G> cudaError_t launch_pack_geom(const PackJob& job, const Launch
   a.stalled_tile = ctx.stalled_tile;
   PackedStatus<unsigned> st;
   st.w = (unsigned long long*)((char*)job.temp + kHeaderBytes);
-  cudaError_t e = cudaMemsetAsync(
-      job.temp, 0, kHeaderBytes + round_up((size_t)rows_tiles<unsigned, G>(1, job.n) * 8, 256), ctx.stream);
-  if (e != cudaSuccess) return e;
   profile_before(ctx);
-  pack_kernel<G><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
+  cudaError_t e = clear_status(job.temp, kHeaderBytes + (size_t)rows_tiles<unsigned, G>(1, job.n) * 8, nullptr, 0, ctx);
+  if (e == cudaSuccess) e = launch_pdl(pack_kernel<G>, a.num_tiles, G::NT, 0, ctx.stream, a, st);
   profile_after(ctx);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_pack(const PackJob& job, const LaunchCtx& ctx) { return launch_pack_geom<PackGeom>(job, ctx); }

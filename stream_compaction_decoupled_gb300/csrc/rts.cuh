@@ -37,6 +37,7 @@ constexpr int kRtsMaxBlocks = 1024;
 
 template <class T, int OP>
 __global__ void __launch_bounds__(256) rts_reduce_kernel(RtsArgs<T> a) {
+  pdl_entry();
   constexpr int NT = 256, VEC = Vec<T>::N, U = 4;
   __shared__ T s_v[NT / 32];
   __shared__ int s_h[NT / 32];
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(256) rts_reduce_kernel(RtsArgs<T> a) {
 
 template <class T, int OP>
 __global__ void __launch_bounds__(kRtsMaxBlocks) rts_spine_kernel(T* partials, int nb) {
+  pdl_entry();
   __shared__ T s_w[32];
   __shared__ T s_incl[kRtsMaxBlocks];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -127,6 +129,7 @@ __global__ void __launch_bounds__(kRtsMaxBlocks) rts_spine_kernel(T* partials, i
 
 template <class T, int OP>
 __global__ void __launch_bounds__(RowsGeom<T>::NT) rts_scan_kernel(RtsArgs<T> a) {
+  pdl_entry();
   using G = RowsGeom<T>;
   constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, TILE = G::TILE;
   __shared__ __align__(128) T s_tile[2][TILE];
@@ -248,12 +251,15 @@ template <class T, int OP> cudaError_t launch_rts_op(const RtsJob& job, const La
   a.vec_ok = ((uintptr_t)job.in % 16 == 0) && ((uintptr_t)job.out % 16 == 0);
   a.err = ctx.err;
   a.wait_ns = ctx.wait_ns;
-  rts_reduce_kernel<T, OP><<<a.nblocks, 256, 0, ctx.stream>>>(a);
-  rts_spine_kernel<T, OP><<<1, kRtsMaxBlocks, 0, ctx.stream>>>(a.partials, a.nblocks);
+  // The three launches follow one another with programmatic dependent launch; the
+  // profile events (when set) bracket all three.
   profile_before(ctx);
-  rts_scan_kernel<T, OP><<<a.nblocks, RowsGeom<T>::NT, 0, ctx.stream>>>(a);
+  cudaError_t e = launch_pdl(rts_reduce_kernel<T, OP>, a.nblocks, 256, 0, ctx.stream, a);
+  if (e == cudaSuccess)
+    e = launch_pdl(rts_spine_kernel<T, OP>, 1, kRtsMaxBlocks, 0, ctx.stream, a.partials, a.nblocks);
+  if (e == cudaSuccess) e = launch_pdl(rts_scan_kernel<T, OP>, a.nblocks, RowsGeom<T>::NT, 0, ctx.stream, a);
   profile_after(ctx);
-  return cudaGetLastError();
+  return e;
 }
 
 template <class T> cudaError_t launch_rts(const RtsJob& job, const LaunchCtx& ctx) {

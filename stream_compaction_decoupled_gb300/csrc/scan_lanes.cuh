@@ -57,6 +57,7 @@ template <class T> using LanesGeom = LanesGeomT<T>;
 
 template <class T, int OP, class S, class Gm = LanesGeom<T>>
 __global__ void __launch_bounds__(Gm::NT) scan_lanes_kernel(LanesArgs<T> a, S st) {
+  pdl_entry();
   constexpr int NT = Gm::NT, NW = Gm::NW, RPG = Gm::RPG;
   __shared__ __align__(128) T s_tile[NT * RPG];
   __shared__ T s_gx[NT];     // group totals, then exclusive group prefixes, [g*CT + c]
@@ -295,16 +296,15 @@ cudaError_t launch_lanes_op(const ScanJob& job, const LaunchCtx& ctx) {
     st.agg = (T*)(status + lanes_flag_bytes(p));
     st.pfx = (T*)(status + lanes_flag_bytes(p) + round_up(lanes_status_entries(p) * sizeof(T), 256));
   }
-  cudaError_t e = cudaMemsetAsync(job.temp, 0, kHeaderBytes, ctx.stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, lanes_flag_bytes(p), ctx.stream);
-  if (e == cudaSuccess && !job.inclusive)
-    e = cudaMemcpyAsync(init_area, job.init_host, (size_t)job.init_lanes * sizeof(T),
-                        cudaMemcpyHostToDevice, ctx.stream);
-  if (e != cudaSuccess) return e;
   profile_before(ctx);
-  scan_lanes_kernel<T, OP, decltype(st), Gm><<<p.num_tiles, Gm::NT, 0, ctx.stream>>>(a, st);
+  cudaError_t e = cudaSuccess;
+  if (!job.inclusive)
+    e = cudaMemcpyAsync(init_area, job.init_host, (size_t)job.init_lanes * sizeof(T), cudaMemcpyHostToDevice,
+                        ctx.stream);
+  if (e == cudaSuccess) e = clear_status(job.temp, kHeaderBytes, status, lanes_flag_bytes(p), ctx);
+  if (e == cudaSuccess) e = launch_pdl(scan_lanes_kernel<T, OP, decltype(st), Gm>, p.num_tiles, Gm::NT, 0, ctx.stream, a, st);
   profile_after(ctx);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace gbs

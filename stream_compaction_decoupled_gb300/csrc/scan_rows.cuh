@@ -62,6 +62,7 @@ using RowsGeom = RowsCfg<T, 128, 8, 2, std::is_same<T, double>::value ? 8 : 12>;
 
 template <class T, int OP, class G, class S>
 __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_kernel(RowsArgs<T> a, S st) {
+  pdl_entry();
   constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, TILE = G::TILE;
   __shared__ __align__(128) T s_tile[TILE];
   __shared__ __align__(8) unsigned long long s_bar;
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_kernel(RowsArgs<T> a
 // about 2.4 operator applications per element instead of ~5.5.
 template <class T, int OP, class G, class S>
 __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_chunk_kernel(RowsArgs<T> a, S st) {
+  pdl_entry();
   constexpr int NT = G::NT, NW = G::NW, CV = G::ROUNDS, VEC = G::VEC, TILE = G::TILE;
   static_assert((CV & (CV - 1)) == 0, "chunk length must be a power of two");
   __shared__ __align__(128) T s_tile[TILE];
@@ -364,17 +366,18 @@ cudaError_t launch_rows_op(const ScanJob& job, const LaunchCtx& ctx) {
   a.wait_ns = ctx.wait_ns;
   a.stalled_tile = ctx.stalled_tile;
   auto st = rows_status<T>(job.temp, a.num_tiles);
-  cudaError_t e = cudaMemsetAsync(job.temp, 0, rows_reset_bytes<T>(a.num_tiles), ctx.stream);
-  if (e != cudaSuccess) return e;
   profile_before(ctx);
-  if constexpr (std::is_same<T, double>::value) {
-    // fp64: thread-contiguous chunks (fewer operator applications).
-    scan_rows_chunk_kernel<T, OP, G, decltype(st)><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
-  } else {
-    scan_rows_kernel<T, OP, G, decltype(st)><<<a.num_tiles, G::NT, 0, ctx.stream>>>(a, st);
+  cudaError_t e = clear_status(job.temp, rows_reset_bytes<T>(a.num_tiles), nullptr, 0, ctx);
+  if (e == cudaSuccess) {
+    if constexpr (std::is_same<T, double>::value) {
+      // fp64: thread-contiguous chunks (fewer operator applications).
+      e = launch_pdl(scan_rows_chunk_kernel<T, OP, G, decltype(st)>, a.num_tiles, G::NT, 0, ctx.stream, a, st);
+    } else {
+      e = launch_pdl(scan_rows_kernel<T, OP, G, decltype(st)>, a.num_tiles, G::NT, 0, ctx.stream, a, st);
+    }
   }
   profile_after(ctx);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace gbs

@@ -254,6 +254,7 @@ __device__ __forceinline__ void seg_chunks(const SegArgsBase& a, unsigned seg, i
 
 template <class T, int OP, class G, class S>
 __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, S st) {
+  pdl_entry();
   constexpr int NW = G::NW, ROUNDS = G::ROUNDS, CH = G::CH;
   __shared__ unsigned s_seg;
   __shared__ T s_warp[NW];
@@ -376,12 +377,11 @@ cudaError_t launch_seg_op(const ScanJob& job, const LaunchCtx& ctx) {
   if (!job.inclusive && job.init_host) memcpy(&a.init, job.init_host, sizeof(T));
   a.inclusive = job.inclusive;
   auto st = seg_status<T>(job.temp);
-  cudaError_t e = cudaMemsetAsync(job.temp, 0, seg_reset_bytes<T>(), ctx.stream);
-  if (e != cudaSuccess) return e;
   profile_before(ctx);
-  scan_seg_kernel<T, OP, G, decltype(st)><<<p.ctas, G::NT, 0, ctx.stream>>>(a, st);
+  cudaError_t e = clear_status(job.temp, seg_reset_bytes<T>(), nullptr, 0, ctx);
+  if (e == cudaSuccess) e = launch_pdl(scan_seg_kernel<T, OP, G, decltype(st)>, p.ctas, G::NT, 0, ctx.stream, a, st);
   profile_after(ctx);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace gbs

@@ -142,6 +142,7 @@ template <class F> __device__ __forceinline__ bool stash_wait(F ready, unsigned 
 
 template <class T, int OP, class S, class C>
 __global__ void __launch_bounds__(C::NT, 1) scan_stash_kernel(StashArgs<T> a, S st) {
+  pdl_entry();
   constexpr int VEC = C::VEC, TILE = C::TILE, RUN = C::RUN, NL = C::NL, QD = C::QD, NR = C::NR;
   constexpr int NSW = C::NSW, NG = C::NG, ROUNDS = C::ROUNDS, NST = 32 * NSW;
   constexpr unsigned FULL = 0xffffffffu;
@@ -576,15 +577,13 @@ cudaError_t launch_stash_op(const ScanJob& job, const LaunchCtx& ctx) {
   auto kern = scan_stash_kernel<T, OP, decltype(st), C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(job.temp, 0,
-                      kHeaderBytes + round_up((size_t)a.num_runs * (sizeof(T) == 4 ? 8 : 4), 256), ctx.stream);
-  if (e != cudaSuccess) return e;
   int grid = ctx.num_sms;
   if ((unsigned)grid > a.num_runs) grid = (int)a.num_runs;
   profile_before(ctx);
-  kern<<<grid, C::NT, C::SMEM, ctx.stream>>>(a, st);
+  e = clear_status(job.temp, kHeaderBytes + (size_t)a.num_runs * (sizeof(T) == 4 ? 8 : 4), nullptr, 0, ctx);
+  if (e == cudaSuccess) e = launch_pdl(kern, grid, C::NT, C::SMEM, ctx.stream, a, st);
   profile_after(ctx);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace gbs
