@@ -56,10 +56,27 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s)"
 
 
-def kernel_source_hash() -> str:
+# The source files each profiled kernel is compiled from: a capture stays valid
+# while none of them changes.
+KERNEL_SOURCES = {
+    "scan_stash_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_stash.cuh"),
+    "scan_rows_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh"),
+    "scan_rows_chunk_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh"),
+    "scan_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh"),
+    "compact_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "compact.cuh"),
+    "compact_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "compact.cuh"),
+    "scan_lanes_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh"),
+    "pack_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "pack.cu"),
+    "rts_scan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "rts.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources of `kernel` (its name up to the first '<')."""
     d = os.path.join(ROOT, "stream_compaction_decoupled_gb300", "csrc")
+    files = KERNEL_SOURCES.get(kernel.split("<")[0], tuple(sorted(os.listdir(d))))
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
+    for f in files:
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -69,12 +86,13 @@ def traffic_from_profiles(kernel: str):
     """DRAM bytes per launch recorded by an ncu capture of this exact kernel source.
 
     The summaries under profiles/ carry 'kernel:', 'source_hash:' and
-    'traffic_bytes_per_launch:' lines; a figure taken on an older source is ignored.
+    'traffic_bytes_per_launch:' lines; a figure taken on older sources of the
+    kernel is ignored.  `python bench.py --source-hash KERNEL` prints the hash.
     """
     d = os.path.join(ROOT, "profiles")
     if not os.path.isdir(d):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(kernel)
     for f in sorted(os.listdir(d)):
         if not f.endswith(".md"):
             continue
@@ -219,10 +237,64 @@ def time_call(fn, reps: int, flush, stream, kernel_events: bool):
             "step_ms_median": float(np.median(steps))}
 
 
+def workload_call(w, device):
+    """The library call of workload `w` on device-resident synthetic inputs:
+    (fn, algorithmic bytes, units, unit)."""
+    import torch
+    import stream_compaction_decoupled_gb300 as gb
+    x = torch.from_numpy(w.make()).to(device)
+    es = x.element_size()
+    if w.kind == "scan":
+        y = torch.empty_like(x)
+        n_el = x.numel()
+        if w.inclusive:
+            fn = lambda: gb.scan_inclusive(x, w.op, lanes=w.lanes, out=y)  # noqa: E731
+        else:
+            fn = lambda: gb.scan_exclusive(x, w.op, lanes=w.lanes, out=y)  # noqa: E731
+        return fn, 2 * n_el * es, n_el // w.lanes, "Gelem/s"
+    if w.kind == "batched":
+        rows, cols = w.shape
+        xv = x.reshape(rows, cols, w.lanes)
+        y = torch.empty_like(xv)
+        fn = lambda: gb.scan_batched(xv, axis=w.axis, op=w.op, lanes=w.lanes, out=y)  # noqa: E731
+        return fn, 2 * x.numel() * es, rows * cols, "Gelem/s"
+    if w.kind == "compact":
+        idx = torch.empty(x.numel(), dtype=torch.int32, device=device)
+        cnt = torch.empty(1, dtype=torch.int32, device=device)
+        p = w.extra["p"]
+        fn = lambda: gb.compact(x, "lt", p, out_idx=idx, out_count=cnt)  # noqa: E731
+        fn()
+        torch.cuda.synchronize()
+        m = int(cnt.item())
+        return fn, 4 * x.numel() + 4 * m + 4, x.numel(), "Gelem/s"
+    total = int(x.sum().item())  # pack
+    recs = torch.empty(total, dtype=torch.int32, device=device)
+    tot = torch.empty(1, dtype=torch.int32, device=device)
+    fn = lambda: gb.pack_by_counts(x, total, offsets=True, out_records=recs, out_total=tot)  # noqa: E731
+    return fn, 4 * x.numel() * 2 + 4 * total, x.numel(), "Gelem/s"
+
+
+def profile_workload(name, reps):
+    """--profile NAME: only that workload's call, 3 untimed calls then `reps` calls
+    with L2 flushed before each, for ncu captures (skip 3 launches, capture 1-3)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from stream_compaction_decoupled_gb300 import workloads as W
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    fn, nbytes, units, unit = workload_call(W.BY_NAME[name], device)
+    for _ in range(3):
+        fn()
+    t = time_call(fn, reps, L2Flush(device), torch.cuda.current_stream(device), kernel_events=True)
+    ms = t["kernel_ms_best"]
+    print(json.dumps({"profile_workload": name, "reps": reps, "call_us_best": round(ms * 1e3, 2),
+                      "GB_s": round(nbytes / (ms * 1e-3) / 1e9, 1)}), flush=True)
+
+
 def secondary_workloads(device, hbm_peak, reps=10, only=None):
     """Every other workload: kernel time, GB/s, fraction of the HBM roofline."""
     import torch
-    import stream_compaction_decoupled_gb300 as gb
     from stream_compaction_decoupled_gb300 import workloads as W
     stream = torch.cuda.current_stream(device)
     flush = L2Flush(device)
@@ -230,37 +302,7 @@ def secondary_workloads(device, hbm_peak, reps=10, only=None):
     for w in W.WORKLOADS:
         if w.name == HEADLINE or (only and w.name not in only):
             continue
-        x = torch.from_numpy(w.make()).to(device)
-        es = x.element_size()
-        if w.kind == "scan":
-            y = torch.empty_like(x)
-            n_el = x.numel()
-            if w.inclusive:
-                fn = lambda: gb.scan_inclusive(x, w.op, lanes=w.lanes, out=y)  # noqa: E731
-            else:
-                fn = lambda: gb.scan_exclusive(x, w.op, lanes=w.lanes, out=y)  # noqa: E731
-            nbytes, units, unit = 2 * n_el * es, n_el // w.lanes, "Gelem/s"
-        elif w.kind == "batched":
-            rows, cols = w.shape
-            xv = x.reshape(rows, cols, w.lanes)
-            y = torch.empty_like(xv)
-            fn = lambda: gb.scan_batched(xv, axis=w.axis, op=w.op, lanes=w.lanes, out=y)  # noqa: E731
-            nbytes, units, unit = 2 * x.numel() * es, rows * cols, "Gelem/s"
-        elif w.kind == "compact":
-            idx = torch.empty(x.numel(), dtype=torch.int32, device=device)
-            cnt = torch.empty(1, dtype=torch.int32, device=device)
-            p = w.extra["p"]
-            fn = lambda: gb.compact(x, "lt", p, out_idx=idx, out_count=cnt)  # noqa: E731
-            fn()
-            torch.cuda.synchronize()
-            m = int(cnt.item())
-            nbytes, units, unit = 4 * x.numel() + 4 * m + 4, x.numel(), "Gelem/s"
-        else:  # pack
-            total = int(x.sum().item())
-            recs = torch.empty(total, dtype=torch.int32, device=device)
-            tot = torch.empty(1, dtype=torch.int32, device=device)
-            fn = lambda: gb.pack_by_counts(x, total, offsets=True, out_records=recs, out_total=tot)  # noqa: E731
-            nbytes, units, unit = 4 * x.numel() * 2 + 4 * total, x.numel(), "Gelem/s"
+        fn, nbytes, units, unit = workload_call(w, device)
         for _ in range(3):
             fn()
         t = time_call(fn, reps, flush, stream, kernel_events=True)
@@ -271,7 +313,7 @@ def secondary_workloads(device, hbm_peak, reps=10, only=None):
                        "GB_s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4),
                        "throughput": round(units / (ms * 1e-3) / 1e9, 3), "throughput_unit": unit,
                        "algorithmic_bytes": int(nbytes), "l2": "flushed between repetitions"}
-        del x
+        del fn
     if only and "fp32_1e8_reduce_then_scan" not in only:
         return out
     # The reduce-then-scan comparison variant on the headline workload.
@@ -492,7 +534,17 @@ def main(argv=None):
                     help="comma-separated names of the other workloads to time (default: all)")
     ap.add_argument("--n", type=int, default=N_HEAD,
                     help="headline size (default 1e8); smaller values are for profiling runs only")
+    ap.add_argument("--profile", metavar="WORKLOAD", default=None,
+                    help="run only WORKLOAD's call (3 untimed, then --steps with L2 flushed) for ncu")
+    ap.add_argument("--source-hash", metavar="KERNEL", default=None,
+                    help="print the source hash that profiles/ summaries of KERNEL record, and exit")
     args = ap.parse_args(argv)
+    if args.source_hash:
+        print(kernel_source_hash(args.source_hash))
+        return
+    if args.profile:
+        profile_workload(args.profile, args.steps)
+        return
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     rank, world, local_rank = dist_init()
