@@ -24,6 +24,15 @@ template <class T> size_t scan_temp_bytes(long long B, long long R, long long C)
 }
 
 template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& ctx) {
+  if constexpr (std::is_same<T, double>::value) {
+    if (seg_chunk_applies<T>(job, ctx.num_sms)) {
+      switch (job.op) {
+        case OP_ADD: return launch_seg_chunk_op<T, OP_ADD>(job, ctx);
+        case OP_MAX: return launch_seg_chunk_op<T, OP_MAX>(job, ctx);
+        default: return launch_seg_chunk_op<T, OP_MIN>(job, ctx);
+      }
+    }
+  }
   if (seg_applies<T>(job)) {
     switch (job.op) {
       case OP_ADD: return launch_seg_op<T, OP_ADD>(job, ctx);

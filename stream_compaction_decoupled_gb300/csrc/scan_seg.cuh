@@ -384,4 +384,251 @@ cudaError_t launch_seg_op(const ScanJob& job, const LaunchCtx& ctx) {
   return e;
 }
 
+// ---- fp64: thread-contiguous chunks ----------------------------------------------
+//
+// GB300 adds fp64 at about 1/70 of its fp32 rate (501.6 G adds/s measured), so an
+// fp64 scan is bound by adds, not bytes, and the layout above (a warp scan per pair
+// of elements) costs about five adds per element.  Here lane l of a warp owns K
+// consecutive elements of each chunk (a chunk is 32 x K elements), reduced serially:
+//   phase 1: lane total (K - 1 adds), kept in shared memory, plus one add into the
+//            warp's running total;
+//   phase 3: a warp scan of the 32 kept lane totals (5 adds), the lane's base (2),
+//            and the seeded serial scan of its K elements (K adds);
+// about 2 + 8/K adds per element in all, against 2 for any work-efficient scan.  The
+// lane's elements are loaded as 16-byte vectors K elements apart across the warp (the
+// L1 cache serves the second half of every 32-byte sector).  Results go out through a
+// per-warp staging buffer so that every store writes whole 128-byte lines (lane-
+// strided 16-byte stores cost L2 eight partial writes per line and made the rescan
+// phase take 1.8x its fp64-add time).
+template <class T, int NT_, int KH_, int NH_, int MAXCPW_, int MINB_> struct SegChunkCfg {
+  static constexpr int NT = NT_, NW = NT_ / 32, MINB = MINB_;
+  static constexpr int VEC = Vec<T>::N;
+  static constexpr int KH = KH_;                 // elements a lane holds in registers at once
+  static constexpr int NH = NH_;                 // register loads per lane per chunk
+  static constexpr int K = KH * NH;              // consecutive elements a lane owns per chunk
+  static constexpr int CH = 32 * K;              // elements per chunk
+  static constexpr int MAXCPW = MAXCPW_;         // chunks a warp can take (shared-memory slots)
+  static constexpr int MAXSEG = 512;
+  static constexpr int M = MAXSEG / 32;
+  static constexpr size_t TOT_BYTES = (size_t)NW * MAXCPW * 32 * sizeof(T);  // kept lane totals
+  static constexpr size_t STAGE_BYTES = (size_t)NW * 32 * KH * sizeof(T);     // output staging
+  static constexpr size_t SMEM = TOT_BYTES + STAGE_BYTES;
+  static_assert(KH % VEC == 0, "whole vectors per lane");
+  static_assert(sizeof(T) != 8 || KH == 16, "the staging swizzle is laid out for 16 doubles a lane");
+};
+// 512 threads (128 registers a thread), 16 doubles a lane, up to 12 chunks a warp
+// (112 KB of shared memory).  Measured on GB300, fp64 add, L2 flushed: 21.2 / 68.3 /
+// 82.6 us at 1e6 / 1e7 / 1.26e7 elements against 31.2 / 115.3 / 133.8 us for the row
+// kernel's chunked variant.
+template <class T> using SegChunkGeom = SegChunkCfg<T, 512, 16, 1, 12, 1>;
+
+template <class T, int KH>
+__device__ __forceinline__ void lane_load(T (&x)[KH], const T* in, long long e0, long long n, unsigned long long pol) {
+  constexpr int VEC = Vec<T>::N;
+  if (e0 + KH <= n) {
+    const uint4* p = reinterpret_cast<const uint4*>(in + e0);
+#pragma unroll
+    for (int j = 0; j < KH / VEC; ++j) {
+      uint4 u;
+      asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                   : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                   : "l"(p + j), "l"(pol));
+      memcpy(&x[j * VEC], &u, 16);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < KH; ++k) x[k] = e0 + k < n ? in[e0 + k] : T{};
+  }
+}
+// Writes the warp's 32 x 16 doubles (lane l's x[] belongs at out + e0 + l * K) as
+// whole lines.  Lane l puts its element k at stage[l*16 + (k ^ (l & 15))]: for a fixed
+// k the 16 lanes of a half-warp hit 16 different 8-byte bank pairs.  Store i then
+// covers the pieces of lanes 4i..4i+3: lane L reads the aligned pair holding elements
+// 2(L%8), 2(L%8)+1 of lane p = 4i + L/8 (swapped when the swizzle is odd) and writes
+// it at its place, so eight lanes write one 128-byte piece.  A piece cut by the end of
+// the input is written element by element.
+template <class T, int K>
+__device__ __forceinline__ void lane_store_staged(const T (&x)[16], T* stage, T* out, long long e_lane0,
+                                                  long long n, int lane, unsigned long long pol) {
+  static_assert(sizeof(T) == 8, "16 doubles a lane");
+  __syncwarp();
+  const int sw = lane & 15;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) stage[lane * 16 + (k ^ sw)] = x[k];
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int pl = 4 * i + (lane >> 3);  // the lane whose piece this is
+    const int k = 2 * (lane & 7);
+    const int ps = pl & 15;
+    const double2 v2 = *reinterpret_cast<const double2*>(&stage[pl * 16 + ((k ^ ps) & ~1)]);
+    T lo, hi;
+    {
+      const double a0 = (ps & 1) ? v2.y : v2.x, a1 = (ps & 1) ? v2.x : v2.y;
+      memcpy(&lo, &a0, 8);
+      memcpy(&hi, &a1, 8);
+    }
+    const long long e = e_lane0 + (long long)pl * K + k;
+    if (e + 2 <= n) {
+      uint4 u;
+      memcpy(&u.x, &lo, 8);
+      memcpy(&u.z, &hi, 8);
+      st_hint(reinterpret_cast<uint4*>(out + e), u, pol);
+    } else {
+      if (e < n) out[e] = lo;
+      if (e + 1 < n) out[e + 1] = hi;
+    }
+  }
+}
+
+template <class T, int OP, class G, class S>
+__global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<T> a, S st) {
+  pdl_entry();
+  constexpr int NW = G::NW, KH = G::KH, NH = G::NH, K = G::K, CH = G::CH, MAXCPW = G::MAXCPW;
+  extern __shared__ __align__(16) unsigned char seg_chunk_smem[];
+  __shared__ unsigned s_seg;
+  __shared__ T s_warp[NW];
+  __shared__ T s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  T* s_tot = reinterpret_cast<T*>(seg_chunk_smem) + warp * MAXCPW * 32;  // [chunk][lane]
+  T* s_stage = reinterpret_cast<T*>(seg_chunk_smem + G::TOT_BYTES) + warp * 32 * KH;
+  if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
+  __syncthreads();
+  const unsigned seg = s_seg;
+  long long c0, c1;
+  seg_chunks(a, seg, warp, NW, c0, c1);
+
+  // Phase 1: lane totals of every chunk (kept), and the warp's total.
+  const unsigned long long keep = l2_policy_evict_last();
+  T acc{};
+  for (long long c = c0; c < c1; ++c) {
+    const long long e0 = c * CH + (long long)lane * K;
+    T t{};
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      T x[KH];
+      lane_load<T, KH>(x, a.in, e0 + h * KH, a.n, keep);
+#pragma unroll
+      for (int k = 0; k < KH; ++k) t = (h == 0 && k == 0) ? x[0] : Op<T, OP>::f(t, x[k]);
+    }
+    s_tot[(c - c0) * 32 + lane] = t;
+    acc = c == c0 ? t : Op<T, OP>::f(acc, t);
+  }
+  const T wtot = warp_allreduce<T, OP>(acc);
+  if (lane == 0) s_warp[warp] = wtot;  // a warp without chunks exists only at the end of the last segment
+  __syncthreads();
+
+  // Phase 2: as in scan_seg_kernel.
+  if (warp == 0) {
+    const T agg = block_scan_warp_totals<T, OP, NW>(s_warp, lane);
+    if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
+    if (seg > 0) {
+      bool timed_out;
+      const T base = seg_gather<T, OP, G::M>(st, seg, a.wait_ns, timed_out);
+      if (lane == 0) {
+        s_base = base;
+        if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+      }
+    }
+  }
+  __syncthreads();
+
+  // Phase 3: per chunk, a warp scan of the kept lane totals seeds each lane's serial
+  // scan of its own elements.
+  bool hb = seg > 0;
+  T base = s_base;
+  if (warp > 0) {
+    const T wp = s_warp[warp - 1];
+    base = hb ? Op<T, OP>::f(base, wp) : wp;
+    hb = true;
+  }
+  if (!a.inclusive) {
+    base = hb ? Op<T, OP>::f(a.init, base) : a.init;
+    hb = true;
+  }
+  const unsigned long long drop = l2_policy_evict_first();
+  for (long long c = c0; c < c1; ++c) {
+    const long long e0 = c * CH + (long long)lane * K;
+    const T t = s_tot[(c - c0) * 32 + lane];
+    const T inc = warp_inclusive<T, OP>(t, lane);
+    const T exc = __shfl_up_sync(0xffffffffu, inc, 1);
+    const T ctot = __shfl_sync(0xffffffffu, inc, 31);
+    T r;
+    bool h;
+    if (lane > 0) {
+      r = hb ? Op<T, OP>::f(base, exc) : exc;
+      h = true;
+    } else {
+      r = base;
+      h = hb;
+    }
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+      T x[KH];
+      lane_load<T, KH>(x, a.in, e0 + hh * KH, a.n, drop);
+      if (a.inclusive) {
+#pragma unroll
+        for (int k = 0; k < KH; ++k) {
+          r = h ? Op<T, OP>::f(r, x[k]) : x[k];
+          h = true;
+          x[k] = r;
+        }
+      } else {  // exclusive: r always holds (the initial value at least)
+#pragma unroll
+        for (int k = 0; k < KH; ++k) {
+          const T v = x[k];
+          x[k] = r;
+          r = Op<T, OP>::f(r, v);
+        }
+      }
+      lane_store_staged<T, K>(x, s_stage, a.out, c * CH + hh * KH, a.n, lane, drop);
+    }
+    base = hb ? Op<T, OP>::f(base, ctot) : ctot;
+    hb = true;
+  }
+}
+
+// The warps' lane totals live in G::MAXCPW shared-memory slots per warp, so a plan
+// whose warps take more chunks than that does not fit this geometry.
+template <class G> bool seg_chunk_plan_fits(const SegPlan& p) {
+  return p.warps > 0 && (p.nc + p.warps - 1) / p.warps <= G::MAXCPW;
+}
+
+template <class T, class G = SegChunkGeom<T>> bool seg_chunk_applies(const ScanJob& job, int num_sms) {
+  if (!(job.B == 1 && job.C == 1 && (uintptr_t)job.in % 16 == 0 && (uintptr_t)job.out % 16 == 0 &&
+        job.R * (long long)sizeof(T) <= kSegMaxBytes))
+    return false;
+  return seg_chunk_plan_fits<G>(seg_plan<G>(job.R, num_sms));
+}
+
+template <class T, int OP, class G = SegChunkGeom<T>>
+cudaError_t launch_seg_chunk_op(const ScanJob& job, const LaunchCtx& ctx) {
+  const SegPlan p = seg_plan<G>(job.R, ctx.num_sms);
+  if (p.ctas == 0) return cudaSuccess;
+  if (!seg_chunk_plan_fits<G>(p)) return cudaErrorInvalidValue;  // callers check seg_chunk_applies
+  SegArgs<T> a;
+  a.n = job.R;
+  a.nc = p.nc;
+  a.warps = p.warps;
+  a.ctas = p.ctas;
+  a.counter = (unsigned*)job.temp;
+  a.err = ctx.err;
+  a.wait_ns = ctx.wait_ns;
+  a.stalled = ctx.stalled_tile;
+  a.in = (const T*)job.in;
+  a.out = (T*)job.out;
+  a.init = T{};
+  if (!job.inclusive && job.init_host) memcpy(&a.init, job.init_host, sizeof(T));
+  a.inclusive = job.inclusive;
+  auto st = seg_status<T>(job.temp);
+  auto kern = scan_seg_chunk_kernel<T, OP, G, decltype(st)>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::SMEM);
+  if (e != cudaSuccess) return e;
+  profile_before(ctx);
+  e = clear_status(job.temp, seg_reset_bytes<T>(), nullptr, 0, ctx);
+  if (e == cudaSuccess) e = launch_pdl(kern, p.ctas, G::NT, G::SMEM, ctx.stream, a, st);
+  profile_after(ctx);
+  return e;
+}
+
 }  // namespace gbs

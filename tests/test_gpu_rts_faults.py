@@ -57,8 +57,8 @@ def stall():
     gb.set_wait_limit_ns(0)
 
 
-@pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "segments", "compact_segments",
-                                  "compact_tiles", "pack", "l2_resident"])
+@pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "segments", "segments_f64",
+                                  "compact_segments", "compact_tiles", "pack", "l2_resident"])
 def test_stalled_tile_times_out(stall, kind):
     n = 64 * 4096 if kind != "l2_resident" else 26_000_000
     x = workloads.uniform01(n, np.float32, 1)
@@ -67,6 +67,8 @@ def test_stalled_tile_times_out(stall, kind):
     if kind == "rows_f32":  # an unaligned view: the row kernel
         gb.scan_inclusive(dev(np.concatenate([x[:1], x]))[1:])
     elif kind == "rows_f64":
+        gb.scan_inclusive(dev(np.concatenate([x[:1], x]).astype(np.float64))[1:])
+    elif kind == "segments_f64":  # 512 chunks of 512 doubles -> 32 segments
         gb.scan_inclusive(dev(x.astype(np.float64)))
     elif kind == "lanes":
         gb.scan_inclusive(dev(x), lanes=8)

@@ -178,15 +178,17 @@ def test_full_size_workload(name):
     assert gb.device_error() == gb.OK
 
 
-# ---- the segment kernel (one aligned row of at most 96 MiB) ------------------------
+# ---- the segment kernels (one aligned row of at most 96 MiB) -----------------------
 # A warp's chunk holds 512 four-byte or 256 eight-byte elements; 152 SMs x 32 warps
 # saturate at 4864 chunks (2,490,368 / 1,245,184 elements), beyond which warps take
-# several chunks.  fp64 stays on the row kernel.
+# several chunks.  fp64 runs the thread-contiguous variant: chunks of 32 lanes x 16
+# doubles, 152 SMs x 16 warps, so 2432 chunks (1,245,184 doubles) saturate it.
 
-SEG_SMALL = [1, 511, 512, 513, 16_384 + 5, 2 * 16_384 + 1, 2_490_368, 2_490_368 + 1, 3_000_017]
+SEG_SMALL = [1, 15, 16, 17, 511, 512, 513, 16_384 + 5, 2 * 16_384 + 1, 1_245_184, 1_245_184 + 1,
+             2_490_368, 2_490_368 + 1, 3_000_017]
 
 
-@pytest.mark.parametrize("dt", ["i32", "u32", "f32", "i64", "u64"])
+@pytest.mark.parametrize("dt", ["i32", "u32", "f32", "i64", "u64", "f64"])
 @pytest.mark.parametrize("op", ["add", "max", "min"])
 @pytest.mark.parametrize("n", SEG_SMALL)
 def test_segment_path(dt, op, n):
@@ -203,7 +205,8 @@ def test_segment_path(dt, op, n):
 
 
 @pytest.mark.parametrize("dt,n", [("f32", 10_000_019), ("i32", 25_165_824), ("f32", 25_165_824),
-                                  ("u64", 12_582_912), ("i64", 7_000_003)])
+                                  ("u64", 12_582_912), ("i64", 7_000_003), ("f64", 10_000_019),
+                                  ("f64", 12_582_912)])
 def test_segment_path_large(dt, n):
     """Up to the 96 MiB limit, where every warp takes several chunks."""
     if dt not in DTYPES:
@@ -218,9 +221,10 @@ def test_segment_path_large(dt, n):
     assert gb.device_error() == gb.OK
 
 
-def test_segment_path_reproducible_and_in_place():
-    """The segment kernel combines in a fixed order: fp32 sums repeat bit for bit."""
-    x = workloads.normal(10_000_000, np.float32, 21)
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_segment_path_reproducible_and_in_place(dt):
+    """The segment kernels combine in a fixed order: float sums repeat bit for bit."""
+    x = workloads.normal(10_000_000, dt, 21)
     xd = to_dev(x)
     first = to_host(gb.scan_inclusive(xd))
     for _ in range(3):
@@ -229,6 +233,19 @@ def test_segment_path_reproducible_and_in_place():
     gb.scan_inclusive(y, out=y)
     assert np.array_equal(to_host(y), first)
     assert gb.device_error() == gb.OK
+
+
+def test_segment_fp64_integer_valued_exact():
+    """Integer-valued doubles sum exactly in any order: the fp64 segment kernel must
+    then agree with the oracle bit for bit, and with the row kernel (unaligned view)."""
+    n = 3_000_017
+    x = workloads.small_ints(n + 1, 4, -50, 51).astype(np.float64)
+    got = to_host(gb.scan_inclusive(to_dev(x[1:])))
+    assert np.array_equal(got, oracle.scan(x[1:]))
+    rows = to_host(gb.scan_inclusive(to_dev(x)[1:]))
+    assert np.array_equal(rows, got)
+    got = to_host(gb.scan_exclusive(to_dev(x[1:]), init=np.float64(7)))
+    assert np.array_equal(got, oracle.scan(x[1:], inclusive=False, init=np.float64(7)))
 
 
 # ---- the L2-resident single-pass path (one long aligned row above 96 MiB) ------------
