@@ -295,6 +295,7 @@ def profile_workload(name, reps):
 def secondary_workloads(device, hbm_peak, reps=10, only=None):
     """Every other workload: kernel time, GB/s, fraction of the HBM roofline."""
     import torch
+    import stream_compaction_decoupled_gb300 as gb
     from stream_compaction_decoupled_gb300 import workloads as W
     stream = torch.cuda.current_stream(device)
     flush = L2Flush(device)

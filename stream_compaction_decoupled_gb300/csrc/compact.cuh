@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
     unsigned base = 0;
     if (seg > 0) {
       bool timed_out;
-      base = seg_gather<unsigned, OP_ADD, G::M>(st, seg, a.wait_ns, timed_out);
+      base = seg_gather<unsigned, OP_ADD, G::M>(st, 0, seg, a.wait_ns, timed_out);
       if (lane == 0 && timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
     }
     if (lane == 0) {
@@ -275,12 +275,13 @@ template <class T> size_t compact_temp_bytes(long long n) {
 
 template <class T> cudaError_t launch_compact_seg(const CompactJob& job, const LaunchCtx& ctx, unsigned predmask) {
   using G = SegGeom<T>;
-  const SegPlan p = seg_plan<G>(job.n, ctx.num_sms);
+  const SegPlan p = seg_plan<G>(1, job.n, ctx.num_sms);
   if (p.ctas == 0) return cudaSuccess;
   CompactSegArgs<T> a;
   a.n = job.n;
   a.nc = p.nc;
   a.warps = p.warps;
+  a.segs = p.segs;
   a.ctas = p.ctas;
   a.counter = (unsigned*)job.temp;
   a.err = ctx.err;

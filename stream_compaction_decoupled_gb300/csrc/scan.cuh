@@ -1,7 +1,8 @@
 // scan.cuh -- dispatch of a scan along the middle axis of a row-major (B, R, C)
-// array.  C == 1 (contiguous rows): one row that fits in L2 goes to the segment
-// kernel, one row many times larger than L2 to the L2-resident look-back kernel,
-// everything else to the row kernel.  C > 1 (lanes / columns): the lane kernel.
+// array.  C == 1 (contiguous rows): one row, or a few long rows, that fit in L2 go
+// to the segment kernel (fp64: its thread-contiguous variant, one row), one row many
+// times larger than L2 to the L2-resident look-back kernel, everything else to the
+// row kernel.  C > 1 (lanes / columns): the lane kernel.
 #pragma once
 
 #include "scan_lanes.cuh"
@@ -16,7 +17,7 @@ template <class T> size_t scan_temp_bytes(long long B, long long R, long long C)
     // Either kernel may run (the choice depends on the pointers' alignment).
     const size_t rows = kHeaderBytes + rows_status_bytes<T>(rows_tiles<T>(B, R));
     const size_t stash = B == 1 ? kHeaderBytes + stash_status_bytes<T>(R) : 0;
-    const size_t seg = B == 1 ? kHeaderBytes + seg_status_bytes<T>() : 0;
+    const size_t seg = kHeaderBytes + seg_status_bytes<T>();
     const size_t m = rows > stash ? rows : stash;
     return m > seg ? m : seg;
   }

@@ -47,28 +47,43 @@ template <class T, int NT_, int ROUNDS_, int MINB_> struct SegCfg {
 };
 template <class T> using SegGeom = SegCfg<T, 1024, 4, 1>;
 
-// Work split: nc chunks over `warps` warps (warp w of the grid takes chunks
-// [w*nc/warps, (w+1)*nc/warps), at least one each), NW warps per CTA.
+// Work split of `rows` independent rows of n elements (a 1-D scan is one row): each
+// row has nc chunks spread over `warps` warps (warp w of a row takes chunks
+// [w*nc/warps, (w+1)*nc/warps), at least one each), NW warps per CTA, `segs` CTAs
+// (segments) per row; segments never cross a row, so a row's scan only gathers its
+// own segments' aggregates.
 struct SegPlan {
+  unsigned rows = 0;
   long long nc = 0;
   unsigned warps = 0;
+  unsigned segs = 0;
   unsigned ctas = 0;
 };
-template <class G> SegPlan seg_plan(long long n, int num_sms) {
+template <class G> SegPlan seg_plan(long long rows, long long n, int num_sms) {
   SegPlan p;
+  if (rows <= 0 || n <= 0) return p;
+  p.rows = (unsigned)rows;
   p.nc = (n + G::CH - 1) / G::CH;
-  long long w = (long long)num_sms * G::MINB * G::NW;
-  if (w > (long long)G::MAXSEG * G::NW) w = (long long)G::MAXSEG * G::NW;
+  long long w = (long long)num_sms * G::MINB * G::NW / rows;
+  if (w < 1) w = 1;
   if (w > p.nc) w = p.nc;
+  long long segs = (w + G::NW - 1) / G::NW;
+  if (segs * rows > G::MAXSEG) {
+    segs = G::MAXSEG / rows;
+    if (segs < 1) return SegPlan{};  // too many rows for the status slots
+    if (w > segs * G::NW) w = segs * G::NW;
+  }
   p.warps = (unsigned)w;
-  p.ctas = (unsigned)((w + G::NW - 1) / G::NW);
+  p.segs = (unsigned)segs;
+  p.ctas = (unsigned)(segs * rows);
   return p;
 }
 
 struct SegArgsBase {
-  long long n;
+  long long n;  // elements per row
   long long nc;
   unsigned warps;
+  unsigned segs;
   unsigned ctas;
   unsigned* counter;
   unsigned* err;
@@ -189,12 +204,15 @@ __device__ __forceinline__ T seg_reduce_part(const T* in, long long n, long long
 }
 
 // Phase 2, by one whole warp: the combination of the aggregates of segments
-// 0..seg-1 (seg >= 1), waiting (bounded by wait_ns) for each to be published.
-// Lane l owns segments l, l+32, ...: all are requested at once, and only those not
-// yet published are read again.  Returns the base sum in every lane.
+// first .. first+cnt-1 (cnt >= 1, the earlier segments of the row), waiting (bounded
+// by wait_ns) for each to be published.  Lane l owns segments first+l, first+l+32,
+// ...: all are requested at once, and only those not yet published are read again.
+// Returns the base sum in every lane.
 template <class T, int OP, int M, class S>
-__device__ __forceinline__ T seg_gather(const S& st, unsigned seg, unsigned long long wait_ns, bool& timed_out) {
+__device__ __forceinline__ T seg_gather(const S& st, unsigned first, unsigned cnt, unsigned long long wait_ns,
+                                        bool& timed_out) {
   const int lane = threadIdx.x & 31;
+  const unsigned seg = cnt;
   T val[M];
   unsigned pending = 0;
 #pragma unroll
@@ -207,9 +225,9 @@ __device__ __forceinline__ T seg_gather(const S& st, unsigned seg, unsigned long
     for (int k = 0; k < M; ++k) {
       if (pending & (1u << k)) {
         T v;
-        const unsigned f = st.poll(lane + 32 * k, v);
+        const unsigned f = st.poll(first + lane + 32 * k, v);
         if (f != FLAG_X) {
-          val[k] = st.fetch(lane + 32 * k, f, v);
+          val[k] = st.fetch(first + lane + 32 * k, f, v);
           pending &= ~(1u << k);
         }
       }
@@ -235,16 +253,17 @@ __device__ __forceinline__ T seg_gather(const S& st, unsigned seg, unsigned long
 #pragma unroll
   for (int k = 1; k < M; ++k)
     if ((unsigned)(lane + 32 * k) < seg) acc = Op<T, OP>::f(acc, val[k]);
-  const T first = __shfl_sync(0xffffffffu, val[0], 0);
-  if ((unsigned)lane >= seg) acc = OP == OP_ADD ? T{} : first;
+  const T v00 = __shfl_sync(0xffffffffu, val[0], 0);
+  if ((unsigned)lane >= seg) acc = OP == OP_ADD ? T{} : v00;
   const T inc = warp_inclusive<T, OP>(acc, lane);
   return __shfl_sync(0xffffffffu, inc, 31);
 }
 
-// The segment's share of the chunks for warp `warp` of the CTA.
-__device__ __forceinline__ void seg_chunks(const SegArgsBase& a, unsigned seg, int warp, int nw, long long& c0,
+// The chunks of the segment's row for warp `warp` of the CTA; `part` is the
+// segment's index within its row.
+__device__ __forceinline__ void seg_chunks(const SegArgsBase& a, unsigned part, int warp, int nw, long long& c0,
                                            long long& c1) {
-  const long long w = (long long)seg * nw + warp;
+  const long long w = (long long)part * nw + warp;
   c0 = c1 = 0;
   if (w < (long long)a.warps) {
     c0 = w * a.nc / a.warps;
@@ -263,22 +282,25 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, 
   if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
   __syncthreads();
   const unsigned seg = s_seg;
+  const unsigned row = seg / a.segs, part = seg - row * a.segs;
+  const T* in = a.in + (long long)row * a.n;
+  T* out = a.out + (long long)row * a.n;
   long long c0, c1;
-  seg_chunks(a, seg, warp, NW, c0, c1);
+  seg_chunks(a, part, warp, NW, c0, c1);
 
   // Phase 1: the warp's total (lanes accumulate their vectors, then one butterfly).
-  const T acc = seg_reduce_part<T, OP, G>(a.in, a.n, c0, c1, lane);
+  const T acc = seg_reduce_part<T, OP, G>(in, a.n, c0, c1, lane);
   const T wtot = warp_allreduce<T, OP>(acc);
-  if (lane == 0) s_warp[warp] = wtot;  // a warp without chunks exists only at the end of the last segment
+  if (lane == 0) s_warp[warp] = wtot;  // a warp without chunks exists only at the end of a row's last segment
   __syncthreads();
 
-  // Phase 2: publish the segment aggregate, gather the earlier ones.
+  // Phase 2: publish the segment aggregate, gather the row's earlier ones.
   if (warp == 0) {
     const T agg = block_scan_warp_totals<T, OP, NW>(s_warp, lane);
     if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
-    if (seg > 0) {
+    if (part > 0) {
       bool timed_out;
-      const T base = seg_gather<T, OP, G::M>(st, seg, a.wait_ns, timed_out);
+      const T base = seg_gather<T, OP, G::M>(st, seg - part, part, a.wait_ns, timed_out);
       if (lane == 0) {
         s_base = base;
         if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
@@ -288,7 +310,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, 
   __syncthreads();
 
   // Phase 3: rescan the warp's chunks from L2, seeded.
-  bool hb = seg > 0;
+  bool hb = part > 0;
   T base = s_base;
   if (warp > 0) {
     const T wp = s_warp[warp - 1];
@@ -301,14 +323,14 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, 
   }
   const unsigned long long drop = l2_policy_evict_first();
   Vec<T> x[ROUNDS];
-  if (c0 < c1) seg_load<T, ROUNDS>(x, a.in, c0 * CH, a.n, lane, drop);
+  if (c0 < c1) seg_load<T, ROUNDS>(x, in, c0 * CH, a.n, lane, drop);
   for (long long c = c0; c < c1; ++c) {
     Vec<T> y[ROUNDS];  // the next chunk, requested before this one is scanned
-    if (c + 1 < c1) seg_load<T, ROUNDS>(y, a.in, (c + 1) * CH, a.n, lane, drop);
+    if (c + 1 < c1) seg_load<T, ROUNDS>(y, in, (c + 1) * CH, a.n, lane, drop);
     T pre[ROUNDS];
     const T ctot = regs_reduce_pass<T, OP, ROUNDS>(x, lane, pre);
     regs_apply_pass<T, OP, ROUNDS>(x, lane, pre, base, hb, a.inclusive);
-    seg_store<T, ROUNDS>(x, a.out, c * CH, a.n, lane, drop);
+    seg_store<T, ROUNDS>(x, out, c * CH, a.n, lane, drop);
     base = hb ? Op<T, OP>::f(base, ctot) : ctot;
     hb = true;
 #pragma unroll
@@ -352,20 +374,29 @@ constexpr long long kSegMaxBytes = 96ll << 20;
 // Not for fp64: this kernel's run layout costs about five fp64 adds per element
 // (warp scans of 2-element vectors), the row kernel's thread-contiguous chunks
 // about 2.4, and fp64 adds, not bytes, bound fp64 scans on GB300.
+// Batched rows (B > 1) come here when they are few and long: each row then gets
+// several CTAs (short rows go to the row kernel, whose tiles never wait across a
+// row); rows must start on 16-byte boundaries.
+constexpr long long kSegMaxRows = 64;
+constexpr long long kSegMinRowElems = 1 << 16;
+
 template <class T> bool seg_applies(const ScanJob& job) {
   if (std::is_same<T, double>::value) return false;
-  return job.B == 1 && job.C == 1 && (uintptr_t)job.in % 16 == 0 && (uintptr_t)job.out % 16 == 0 &&
-         job.R * (long long)sizeof(T) <= kSegMaxBytes;
+  if (job.C != 1 || job.B < 1 || (uintptr_t)job.in % 16 != 0 || (uintptr_t)job.out % 16 != 0) return false;
+  if (job.B * job.R * (long long)sizeof(T) > kSegMaxBytes) return false;
+  if (job.B == 1) return true;
+  return job.B <= kSegMaxRows && job.R >= kSegMinRowElems && (job.R * (long long)sizeof(T)) % 16 == 0;
 }
 
 template <class T, int OP, class G = SegGeom<T>>
 cudaError_t launch_seg_op(const ScanJob& job, const LaunchCtx& ctx) {
-  const SegPlan p = seg_plan<G>(job.R, ctx.num_sms);
-  if (p.ctas == 0) return cudaSuccess;
+  const SegPlan p = seg_plan<G>(job.B, job.R, ctx.num_sms);
+  if (p.ctas == 0) return cudaErrorInvalidValue;  // callers check seg_applies
   SegArgs<T> a;
   a.n = job.R;
   a.nc = p.nc;
   a.warps = p.warps;
+  a.segs = p.segs;
   a.ctas = p.ctas;
   a.counter = (unsigned*)job.temp;
   a.err = ctx.err;
@@ -494,7 +525,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<
   T* s_stage = reinterpret_cast<T*>(seg_chunk_smem + G::TOT_BYTES) + warp * 32 * KH;
   if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
   __syncthreads();
-  const unsigned seg = s_seg;
+  const unsigned seg = s_seg;  // one row: the segment is its part
   long long c0, c1;
   seg_chunks(a, seg, warp, NW, c0, c1);
 
@@ -524,7 +555,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<
     if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
     if (seg > 0) {
       bool timed_out;
-      const T base = seg_gather<T, OP, G::M>(st, seg, a.wait_ns, timed_out);
+      const T base = seg_gather<T, OP, G::M>(st, 0, seg, a.wait_ns, timed_out);
       if (lane == 0) {
         s_base = base;
         if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
@@ -598,18 +629,18 @@ template <class T, class G = SegChunkGeom<T>> bool seg_chunk_applies(const ScanJ
   if (!(job.B == 1 && job.C == 1 && (uintptr_t)job.in % 16 == 0 && (uintptr_t)job.out % 16 == 0 &&
         job.R * (long long)sizeof(T) <= kSegMaxBytes))
     return false;
-  return seg_chunk_plan_fits<G>(seg_plan<G>(job.R, num_sms));
+  return seg_chunk_plan_fits<G>(seg_plan<G>(1, job.R, num_sms));
 }
 
 template <class T, int OP, class G = SegChunkGeom<T>>
 cudaError_t launch_seg_chunk_op(const ScanJob& job, const LaunchCtx& ctx) {
-  const SegPlan p = seg_plan<G>(job.R, ctx.num_sms);
-  if (p.ctas == 0) return cudaSuccess;
-  if (!seg_chunk_plan_fits<G>(p)) return cudaErrorInvalidValue;  // callers check seg_chunk_applies
+  const SegPlan p = seg_plan<G>(1, job.R, ctx.num_sms);
+  if (p.ctas == 0 || !seg_chunk_plan_fits<G>(p)) return cudaErrorInvalidValue;  // callers check seg_chunk_applies
   SegArgs<T> a;
   a.n = job.R;
   a.nc = p.nc;
   a.warps = p.warps;
+  a.segs = p.segs;
   a.ctas = p.ctas;
   a.counter = (unsigned*)job.temp;
   a.err = ctx.err;

@@ -46,6 +46,33 @@ def test_rows_axis1(dt, op, shape):
     assert_scan_matches(got, as3(x, rows, cols, 1), op, False, init, what="axis1 excl %s" % (shape,))
 
 
+# Few long rows (B <= 64, at least 65536 elements, 16-byte rows, at most 96 MiB in
+# all) take the segment kernel with segments per row; the other shapes here sit just
+# outside those limits and take the row kernel.
+@pytest.mark.parametrize("dt", ["i32", "f32", "i64"])
+@pytest.mark.parametrize("op", ["add", "max", "min"])
+@pytest.mark.parametrize("shape", [(2, 65536), (3, 65536 + 4), (64, 65536), (5, 1_000_004), (65, 65536),
+                                   (5, 1_000_003), (3, 65532)])
+def test_rows_axis1_segments(dt, op, shape):
+    rows, cols = shape
+    x = make(dt, rows * cols, rows * 17 + cols)
+    xd = dev(x).reshape(rows, cols)
+    got = gb.scan_batched(xd, axis=1, op=op).cpu().numpy()
+    assert_scan_matches(got, as3(x, rows, cols, 1), op, True, what="seg rows %s %s %s" % (dt, op, shape))
+    init = x[0] if op != "add" else 5
+    got = gb.scan_batched(xd, axis=1, op=op, inclusive=False, init=init).cpu().numpy()
+    assert_scan_matches(got, as3(x, rows, cols, 1), op, False, init, what="seg rows excl %s" % (shape,))
+    assert gb.device_error() == gb.OK
+
+
+def test_rows_axis1_above_segment_limit():
+    """2 rows of 12,582,912 fp32 (100.7 MB in all, above 96 MiB) take the row kernel."""
+    rows, cols = 2, 12_582_912
+    x = make("f32", rows * cols, 99)
+    got = gb.scan_batched(dev(x).reshape(rows, cols), axis=1).cpu().numpy()
+    assert_scan_matches(got, as3(x, rows, cols, 1), "add", True, what="rows kernel 2 x 12.6M")
+
+
 @pytest.mark.parametrize("dt", ["i32", "f32", "f64", "i64"])
 @pytest.mark.parametrize("op", ["add", "min"])
 @pytest.mark.parametrize("shape", [(1, 7), (5, 3), (513, 8), (1000, 17), (130, 24), (65, 64), (200, 65),
