@@ -119,6 +119,30 @@ def test_lane_vectors_along_rows(lanes):
     assert_scan_matches(got, as3(x, 1, rows, cols * lanes), "add", True, what="columns of lane vectors")
 
 
+# ---- lane-vector scans over many tiles: one tile, several waves of tiles, ragged last
+# tiles, batches, 16-byte and odd row widths (tiles hold 320 rows of 24 fp32 lanes, 1024
+# rows of 8, 480 rows of 17 fp64 lanes).
+
+LANE_SHAPES = [(1, 320, 24), (1, 321, 24), (1, 200_000, 24), (3, 100_003, 24), (1, 1_000_000, 8),
+               (2, 4097, 8), (1, 300_000, 17), (5, 20_000, 17), (1, 150_000, 32), (1, 40_000, 64),
+               (1, 50_000, 65), (2, 10_001, 6)]
+
+
+@pytest.mark.parametrize("dt", ["f32", "f64", "i32", "i64"])
+@pytest.mark.parametrize("op", ["add", "max"])
+@pytest.mark.parametrize("shape", LANE_SHAPES)
+def test_lane_tiles(dt, op, shape):
+    b, n, lanes = shape
+    x = make(dt, b * n * lanes, b * n + lanes)
+    xd = dev(x).reshape(b, n, lanes)
+    got = gb.scan_batched(xd, axis=1, op=op, lanes=lanes).cpu().numpy()
+    assert_scan_matches(got, as3(x, b, n, lanes), op, True, what="lanes %s %s %s" % (dt, op, shape))
+    init = (np.arange(lanes) - 3).astype(NP[dt]) if op == "add" else x[:lanes].copy()
+    got = gb.scan_batched(xd, axis=1, op=op, inclusive=False, init=init, lanes=lanes).cpu().numpy()
+    assert_scan_matches(got, as3(x, b, n, lanes), op, False, init, what="lanes excl %s" % (shape,))
+    assert gb.device_error() == gb.OK
+
+
 # ---- the full-size batched and large-element workloads, element by element -------
 
 BATCHED = ["fp32_4096x4096_axis0", "fp32_4096x4096_axis1", "fp32_2x1e7_axis1", "fp32_1e6x8_axis0",

@@ -57,7 +57,7 @@ def stall():
     gb.set_wait_limit_ns(0)
 
 
-@pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "segments", "segments_f64",
+@pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "lanes_wide", "segments", "segments_f64",
                                   "compact_segments", "compact_tiles", "pack", "l2_resident"])
 def test_stalled_tile_times_out(stall, kind):
     n = 64 * 4096 if kind != "l2_resident" else 26_000_000
@@ -72,6 +72,8 @@ def test_stalled_tile_times_out(stall, kind):
         gb.scan_inclusive(dev(x.astype(np.float64)))
     elif kind == "lanes":
         gb.scan_inclusive(dev(x), lanes=8)
+    elif kind == "lanes_wide":  # 65 lanes: 64-lane strips
+        gb.scan_inclusive(dev(x[: n // 65 * 65]), lanes=65)
     elif kind == "segments":  # 512 chunks -> 16 segments; segment 3 never publishes
         gb.scan_inclusive(dev(x))
     elif kind == "l2_resident":  # one long row: the stalled index is a run of 4 tiles
