@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
   __syncthreads();
   const unsigned seg = s_seg;
   long long c0, c1;
-  seg_chunks(a, seg, warp, NW, c0, c1);
+  const int nact = seg_chunks(a, seg, warp, NW, c0, c1);
 
   // Phase 1: selected elements in the warp's part (coalesced vectors, U per lane in
   // flight, L2 evict-last so that phase 3 finds them).
@@ -188,24 +188,19 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
     const long long v1 = e1 / VEC;
     const uint4* p = reinterpret_cast<const uint4*>(a.in);
     long long v = c0 * CH / VEC + lane;
-    for (; v + 32 * (U - 1) < v1; v += 32 * U) {
+    for (; v < v1; v += 32 * U) {  // U loads in flight, the last round guarded
       uint4 u[U];
 #pragma unroll
-      for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
+      for (int k = 0; k < U; ++k)
+        if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
 #pragma unroll
       for (int k = 0; k < U; ++k) {
+        if (v + 32 * k >= v1) break;
         Vec<T> x;
         memcpy(x.v, &u[k], 16);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) cnt += selects(x.v[e], a.thr, a.predmask) ? 1u : 0u;
       }
-    }
-    for (; v < v1; v += 32) {
-      const uint4 u = ld_hint(p + v, keep);
-      Vec<T> x;
-      memcpy(x.v, &u, 16);
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) cnt += selects(x.v[e], a.thr, a.predmask) ? 1u : 0u;
     }
     if (lane == 0)
       for (long long i = v1 * VEC; i < e1; ++i) cnt += selects(a.in[i], a.thr, a.predmask) ? 1u : 0u;
@@ -216,7 +211,9 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
 
   // Phase 2: publish the segment's count, gather the earlier counts.
   if (warp == 0) {
-    const unsigned agg = block_scan_warp_totals<unsigned, OP_ADD, NW>(s_warp, lane);
+    block_scan_warp_totals<unsigned, OP_ADD, NW>(s_warp, lane);
+    __syncwarp();
+    const unsigned agg = s_warp[nact - 1];
     if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
     unsigned base = 0;
     if (seg > 0) {
@@ -280,7 +277,6 @@ template <class T> cudaError_t launch_compact_seg(const CompactJob& job, const L
   CompactSegArgs<T> a;
   a.n = job.n;
   a.nc = p.nc;
-  a.warps = p.warps;
   a.segs = p.segs;
   a.ctas = p.ctas;
   a.counter = (unsigned*)job.temp;

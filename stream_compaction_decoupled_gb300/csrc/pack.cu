@@ -1,18 +1,20 @@
-// pack.cu -- variable-length output packing by counts in one pass (B. Merry,
+// pack.cu -- variable-length output packing by counts in one launch (B. Merry,
 // "Prefix sums on GPUs", slides "Output Format" and "Solution": every object
 // counts its records, the counts are exclusive-scanned into start positions, and
 // every object emits its records at its position).
 //
-// Per tile of 4096 counts (row-scan geometry, claimed in order): bulk-copy the
-// counts into shared memory; exclusive-scan them there (pass 1, block scan,
-// decoupled look-back over packed (flag, running total) words, pass 2); write the
-// global start offsets if asked; then emit the tile's records contiguously: each
-// thread takes runs of consecutive output slots of the tile, finds the object owning
-// the first by a binary search over the tile's local offsets and walks forward, so
-// the work per record is constant whatever the count distribution.  Offsets add
-// with saturation at 2^31 so a total that does not fit int32 is caught, not
-// wrapped.
+// Two kernels.  Counts that fit in L2 (16-byte aligned, up to 96 MiB) take the
+// segment kernel below (pack_seg_kernel).  Otherwise, per tile of 1024 counts (row-
+// scan geometry, claimed in order): bulk-copy the counts into shared memory;
+// exclusive-scan them there (pass 1, block scan, decoupled look-back over packed
+// (flag, running total) words, pass 2); write the global start offsets if asked; then
+// emit the tile's records contiguously: each thread takes runs of consecutive output
+// slots of the tile, finds the object owning the first by a binary search over the
+// tile's local offsets and walks forward, so the work per record is constant
+// whatever the count distribution.  In both, offsets add with saturation at 2^31 so
+// a total that does not fit int32 is caught, not wrapped.
 #include "scan_rows.cuh"
+#include "scan_seg.cuh"
 
 namespace gbs {
 
@@ -182,8 +184,221 @@ __global__ void __launch_bounds__(G::NT, G::MINB) pack_kernel(PackArgs a, Packed
 // a quarter of the scans' (1024 counts: four times as many CTAs share the emission).
 using PackGeom = RowsCfg<unsigned, 128, 2, 2, 12>;
 
+// ---- packing for inputs that fit in L2: the segment scheme (scan_seg.cuh) ----------
+//
+// Phase 1 sums each warp's counts (negative counts read as 0; 64-bit sums capped at
+// 2^31, which is the saturating add of the counts), phase 2 publishes the segment
+// sum and gathers the earlier ones, phase 3 walks the warp's chunks again from L2:
+// the exclusive offsets of a chunk (saturating, seeded with the running base) are
+// written out and kept in shared memory, and the chunk's records are emitted in
+// blocks of 32 x PV output slots: lane l takes PV consecutive slots, finds the object
+// owning the first by a binary search over the kept offsets and walks forward (an
+// object without records shares its successor's offset and is stepped over), writes
+// the owners to a per-warp staging buffer (lane l's slot v at l*PV + (v ^ ((l/4) mod
+// PV)): the lanes' writes and the block's reads both hit 32 different banks), and the
+// warp stores the block contiguously.  Measured on GB300 for 1e6 Poisson(4) counts:
+// 20.6 us (8 slots a lane; 16 give 20.9 us) against 42.8 us for the tile kernel.
+constexpr int PV = 8;
+constexpr int PSW = 2;  // log2(32 / PV): lanes l and l + 32/PV share a bank row
+// Chunks of 128 counts (one 16-byte vector a lane): about 512 records each for the
+// Poisson(4) workload, so that a million counts give every warp of every SM chunks
+// to emit (emission is instruction-bound, not memory-bound).
+using PackSegGeom = SegCfg<unsigned, 1024, 1, 1>;
+constexpr size_t kPackSegSmem = (size_t)PackSegGeom::NW * (PackSegGeom::CH + 32 * PV) * sizeof(unsigned);
+
+struct PackSegArgs : SegArgsBase {
+  const int* counts;
+  int* offsets;  // nullable
+  int* records;
+  long long capacity;
+  int* out_total;
+};
+
+__global__ void __launch_bounds__(PackSegGeom::NT, PackSegGeom::MINB) pack_seg_kernel(PackSegArgs a,
+                                                                                    PackedStatus<unsigned> st) {
+  pdl_entry();
+  using G = PackSegGeom;
+  constexpr int NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, CH = G::CH;
+  constexpr unsigned CAP = 0x80000000u;  // offsets saturate here
+  extern __shared__ __align__(16) unsigned pack_seg_smem[];
+  __shared__ unsigned s_seg;
+  __shared__ unsigned s_warp[NW];
+  __shared__ unsigned s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned* s_off = pack_seg_smem + warp * (CH + 32 * PV);  // the chunk's offsets
+  unsigned* s_stage = s_off + CH;                            // one block of owners
+  if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
+  __syncthreads();
+  const unsigned seg = s_seg;
+  long long c0, c1;
+  const int nact = seg_chunks(a, seg, warp, NW, c0, c1);
+
+  // Phase 1: the warp's count sum.
+  {
+    constexpr int U = 8;
+    const unsigned long long keep = l2_policy_evict_last();
+    const long long e1 = c1 * CH < a.n ? c1 * CH : a.n;
+    const long long v1 = e1 / VEC;
+    const uint4* p = reinterpret_cast<const uint4*>(a.counts);
+    unsigned long long sum = 0;
+    long long v = c0 * CH / VEC + lane;
+    for (; v < v1; v += 32 * U) {  // U loads in flight, the last round guarded
+      uint4 u[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k)
+        if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        if (v + 32 * k >= v1) break;
+        sum += (unsigned long long)(unsigned)max((int)u[k].x, 0) + (unsigned)max((int)u[k].y, 0) +
+               (unsigned)max((int)u[k].z, 0) + (unsigned)max((int)u[k].w, 0);
+      }
+    }
+    if (lane == 0)
+      for (long long i = v1 * VEC; i < e1; ++i) sum += (unsigned)max(a.counts[i], 0);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) s_warp[warp] = sum >= CAP ? CAP : (unsigned)sum;
+  }
+  __syncthreads();
+
+  // Phase 2: publish the segment's sum, gather the earlier sums; the last segment
+  // writes the total.
+  if (warp == 0) {
+    block_scan_warp_totals<unsigned, OP_SATADD, NW>(s_warp, lane);
+    __syncwarp();
+    const unsigned agg = s_warp[nact - 1];
+    if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
+    unsigned base = 0;
+    if (seg > 0) {
+      bool timed_out;
+      base = seg_gather<unsigned, OP_SATADD, G::M>(st, 0, seg, a.wait_ns, timed_out);
+      if (lane == 0 && timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+    }
+    if (lane == 0) {
+      s_base = base;
+      if (seg == a.ctas - 1) {
+        const unsigned total = Op<unsigned, OP_SATADD>::f(base, agg);
+        *a.out_total = total >= CAP ? 0x7fffffff : (int)total;
+        if (total >= CAP || (long long)total > a.capacity) atomicOr(a.err, ERRBIT_RANGE);
+      }
+    }
+  }
+  __syncthreads();
+
+  // Phase 3: offsets and records, chunk by chunk.
+  unsigned run = s_base;
+  if (warp > 0) run = Op<unsigned, OP_SATADD>::f(run, s_warp[warp - 1]);
+  const unsigned long long drop = l2_policy_evict_first();
+  bool negative = false;
+  for (long long c = c0; c < c1; ++c) {
+    Vec<unsigned> x[ROUNDS];
+    seg_load<unsigned, ROUNDS>(x, reinterpret_cast<const unsigned*>(a.counts), c * CH, a.n, lane, drop);
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e)
+        if ((int)x[j].v[e] < 0) {
+          x[j].v[e] = 0;
+          negative = true;
+        }
+    unsigned pre[ROUNDS];
+    const unsigned ctot = regs_reduce_pass<unsigned, OP_SATADD, ROUNDS>(x, lane, pre);
+    regs_apply_pass<unsigned, OP_SATADD, ROUNDS>(x, lane, pre, run, true, false);  // x: exclusive offsets
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < ROUNDS; ++j) {
+      st_vec<unsigned>(reinterpret_cast<uint4*>(s_off) + j * 32 + lane, x[j]);
+      if (a.offsets) {
+        const long long e0 = c * CH + (long long)(j * 32 + lane) * VEC;
+        Vec<unsigned> o;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) o.v[e] = x[j].v[e] >= CAP ? 0x7fffffffu : x[j].v[e];
+        if (e0 + VEC <= a.n && ((uintptr_t)(a.offsets + e0) & 15) == 0) {
+          uint4 u;
+          memcpy(&u, o.v, 16);
+          st_hint(reinterpret_cast<uint4*>(a.offsets + e0), u, drop);
+        } else {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e)
+            if (e0 + e < a.n) a.offsets[e0 + e] = (int)o.v[e];
+        }
+      }
+    }
+    __syncwarp();
+    // Records of this chunk: slots [run, run + ctot), capped by the capacity (slots
+    // and offsets stay below 2^31, so 32-bit arithmetic suffices).
+    const unsigned cend_u = Op<unsigned, OP_SATADD>::f(run, ctot);
+    const unsigned cb = run, ce = (long long)cend_u < a.capacity ? cend_u : (unsigned)a.capacity;
+    const unsigned obj0 = (unsigned)(c * CH);
+    for (unsigned b0 = cb; b0 < ce; b0 += 32 * PV) {
+      const unsigned s0 = b0 + (unsigned)lane * PV;
+      if (s0 < ce) {
+        int lo = 0, hi = CH;  // the last object with offset <= s0
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (s_off[mid] <= s0) lo = mid;
+          else hi = mid;
+        }
+        int obj = lo;
+#pragma unroll
+        for (int v = 0; v < PV; ++v) {
+          const unsigned sl = s0 + v;
+          while (obj + 1 < CH && s_off[obj + 1] <= sl) ++obj;
+          s_stage[lane * PV + (v ^ ((lane >> PSW) & (PV - 1)))] = obj0 + obj;
+        }
+      }
+      __syncwarp();
+      const unsigned nblk = ce - b0 < 32u * PV ? ce - b0 : 32u * PV;
+      int* dst = a.records + b0;
+#pragma unroll
+      for (int i = 0; i < PV; ++i) {
+        const unsigned k = (unsigned)(lane + 32 * i);
+        const unsigned ln = k / PV, v = k % PV;
+        if (k < nblk) dst[k] = (int)s_stage[ln * PV + (v ^ ((ln >> PSW) & (PV - 1)))];
+      }
+      __syncwarp();
+    }
+    run = cend_u;
+  }
+  if (negative) atomicOr(a.err, ERRBIT_INVALID);
+}
+
 size_t pack_temp_bytes(long long n) {
-  return kHeaderBytes + round_up((size_t)rows_tiles<unsigned, PackGeom>(1, n) * 8, 256);
+  const size_t rows = kHeaderBytes + round_up((size_t)rows_tiles<unsigned, PackGeom>(1, n) * 8, 256);
+  const size_t seg = kHeaderBytes + seg_status_bytes<unsigned>();
+  return rows > seg ? rows : seg;
+}
+
+// Inputs up to this many counts take the segment kernel (16-byte aligned counts).
+constexpr long long kPackSegMaxCounts = (96ll << 20) / 4;
+
+cudaError_t launch_pack_seg(const PackJob& job, const LaunchCtx& ctx) {
+  using G = PackSegGeom;
+  const SegPlan p = seg_plan<G>(1, job.n, ctx.num_sms);
+  if (p.ctas == 0) return cudaErrorInvalidValue;
+  PackSegArgs a;
+  a.n = job.n;
+  a.nc = p.nc;
+  a.segs = p.segs;
+  a.ctas = p.ctas;
+  a.counter = (unsigned*)job.temp;
+  a.err = ctx.err;
+  a.wait_ns = ctx.wait_ns;
+  a.stalled = ctx.stalled_tile;
+  a.counts = job.counts;
+  a.offsets = job.offsets;
+  a.records = job.records;
+  a.capacity = job.capacity;
+  a.out_total = job.out_total;
+  PackedStatus<unsigned> st = seg_status<unsigned>(job.temp);
+  cudaError_t e = cudaFuncSetAttribute(pack_seg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPackSegSmem);
+  if (e != cudaSuccess) return e;
+  profile_before(ctx);
+  e = clear_status(job.temp, seg_reset_bytes<unsigned>(), nullptr, 0, ctx);
+  if (e == cudaSuccess) e = launch_pdl(pack_seg_kernel, p.ctas, G::NT, kPackSegSmem, ctx.stream, a, st);
+  profile_after(ctx);
+  return e;
 }
 
 template <class G> cudaError_t launch_pack_geom(const PackJob& job, const LaunchCtx& ctx) {
@@ -210,6 +425,9 @@ template <class G> cudaError_t launch_pack_geom(const PackJob& job, const Launch
   return e;
 }
 
-cudaError_t launch_pack(const PackJob& job, const LaunchCtx& ctx) { return launch_pack_geom<PackGeom>(job, ctx); }
+cudaError_t launch_pack(const PackJob& job, const LaunchCtx& ctx) {
+  if ((uintptr_t)job.counts % 16 == 0 && job.n <= kPackSegMaxCounts) return launch_pack_seg(job, ctx);
+  return launch_pack_geom<PackGeom>(job, ctx);
+}
 
 }  // namespace gbs

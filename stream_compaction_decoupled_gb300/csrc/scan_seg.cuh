@@ -48,41 +48,41 @@ template <class T, int NT_, int ROUNDS_, int MINB_> struct SegCfg {
 template <class T> using SegGeom = SegCfg<T, 1024, 4, 1>;
 
 // Work split of `rows` independent rows of n elements (a 1-D scan is one row): each
-// row has nc chunks spread over `warps` warps (warp w of a row takes chunks
-// [w*nc/warps, (w+1)*nc/warps), at least one each), NW warps per CTA, `segs` CTAs
-// (segments) per row; segments never cross a row, so a row's scan only gathers its
-// own segments' aggregates.
+// row's nc chunks are spread over `segs` segments (CTAs; segment p of a row takes
+// chunks [p*nc/segs, (p+1)*nc/segs), at least one), then over the segment's NW warps
+// (the first k mod NW warps take one chunk more, so warps without chunks come last).
+// Spreading over CTAs first keeps every SM busy when there are fewer chunks than
+// warps.  Segments never cross a row, so a row's scan only gathers its own segments'
+// aggregates.
 struct SegPlan {
   unsigned rows = 0;
-  long long nc = 0;
-  unsigned warps = 0;
-  unsigned segs = 0;
+  long long nc = 0;   // chunks per row
+  unsigned segs = 0;  // segments per row
   unsigned ctas = 0;
+  long long cpw = 0;  // most chunks any warp takes
 };
 template <class G> SegPlan seg_plan(long long rows, long long n, int num_sms) {
   SegPlan p;
   if (rows <= 0 || n <= 0) return p;
   p.rows = (unsigned)rows;
   p.nc = (n + G::CH - 1) / G::CH;
-  long long w = (long long)num_sms * G::MINB * G::NW / rows;
-  if (w < 1) w = 1;
-  if (w > p.nc) w = p.nc;
-  long long segs = (w + G::NW - 1) / G::NW;
+  long long segs = (long long)num_sms * G::MINB / rows;
+  if (segs < 1) segs = 1;
+  if (segs > p.nc) segs = p.nc;
   if (segs * rows > G::MAXSEG) {
     segs = G::MAXSEG / rows;
     if (segs < 1) return SegPlan{};  // too many rows for the status slots
-    if (w > segs * G::NW) w = segs * G::NW;
   }
-  p.warps = (unsigned)w;
   p.segs = (unsigned)segs;
   p.ctas = (unsigned)(segs * rows);
+  const long long cps = (p.nc + segs - 1) / segs;  // most chunks in a segment
+  p.cpw = (cps + G::NW - 1) / G::NW;
   return p;
 }
 
 struct SegArgsBase {
   long long n;  // elements per row
   long long nc;
-  unsigned warps;
   unsigned segs;
   unsigned ctas;
   unsigned* counter;
@@ -179,24 +179,19 @@ __device__ __forceinline__ T seg_reduce_part(const T* in, long long n, long long
     for (int e = 1; e < VEC; ++e) acc = Op<T, OP>::f(acc, x.v[e]);
     v += 32;
   }
-  for (; v + 32 * (U - 1) < v1; v += 32 * U) {
+  for (; v < v1; v += 32 * U) {  // U loads in flight, the last round guarded
     uint4 u[U];
 #pragma unroll
-    for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
+    for (int k = 0; k < U; ++k)
+      if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
 #pragma unroll
     for (int k = 0; k < U; ++k) {
+      if (v + 32 * k >= v1) break;
       Vec<T> x;
       memcpy(x.v, &u[k], 16);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) acc = Op<T, OP>::f(acc, x.v[e]);
     }
-  }
-  for (; v < v1; v += 32) {
-    const uint4 u = ld_hint(p + v, keep);
-    Vec<T> x;
-    memcpy(x.v, &u, 16);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) acc = Op<T, OP>::f(acc, x.v[e]);
   }
   if (lane == 0)
     for (long long i = v1 * VEC; i < e1; ++i) acc = Op<T, OP>::f(acc, in[i]);
@@ -247,28 +242,28 @@ __device__ __forceinline__ T seg_gather(const S& st, unsigned first, unsigned cn
     backoff(spins);
   }
   // Lane fold in segment order, then the lanes in lane order.  A lane with no
-  // segment contributes the identity of add, or (max / min being idempotent) lane
-  // 0's first value.
+  // segment contributes the identity of add (and of the saturating add), or (max /
+  // min being idempotent) lane 0's first value.
   T acc = val[0];
 #pragma unroll
   for (int k = 1; k < M; ++k)
     if ((unsigned)(lane + 32 * k) < seg) acc = Op<T, OP>::f(acc, val[k]);
   const T v00 = __shfl_sync(0xffffffffu, val[0], 0);
-  if ((unsigned)lane >= seg) acc = OP == OP_ADD ? T{} : v00;
+  if ((unsigned)lane >= seg) acc = (OP == OP_ADD || OP == OP_SATADD) ? T{} : v00;
   const T inc = warp_inclusive<T, OP>(acc, lane);
   return __shfl_sync(0xffffffffu, inc, 31);
 }
 
-// The chunks of the segment's row for warp `warp` of the CTA; `part` is the
-// segment's index within its row.
-__device__ __forceinline__ void seg_chunks(const SegArgsBase& a, unsigned part, int warp, int nw, long long& c0,
-                                           long long& c1) {
-  const long long w = (long long)part * nw + warp;
-  c0 = c1 = 0;
-  if (w < (long long)a.warps) {
-    c0 = w * a.nc / a.warps;
-    c1 = (w + 1) * a.nc / a.warps;
-  }
+// The chunks [c0, c1) of the segment's row for warp `warp` of the CTA, `part` being
+// the segment's index within its row; returns how many of the CTA's warps have
+// chunks (they are the first ones).
+__device__ __forceinline__ int seg_chunks(const SegArgsBase& a, unsigned part, int warp, int nw, long long& c0,
+                                          long long& c1) {
+  const long long cb = (long long)part * a.nc / a.segs, ce = (long long)(part + 1) * a.nc / a.segs;
+  const long long k = ce - cb, q = k / nw, r = k % nw;
+  c0 = cb + warp * q + (warp < r ? warp : r);
+  c1 = c0 + q + (warp < r ? 1 : 0);
+  return k < nw ? (int)k : nw;
 }
 
 template <class T, int OP, class G, class S>
@@ -286,17 +281,19 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, 
   const T* in = a.in + (long long)row * a.n;
   T* out = a.out + (long long)row * a.n;
   long long c0, c1;
-  seg_chunks(a, part, warp, NW, c0, c1);
+  const int nact = seg_chunks(a, part, warp, NW, c0, c1);
 
   // Phase 1: the warp's total (lanes accumulate their vectors, then one butterfly).
   const T acc = seg_reduce_part<T, OP, G>(in, a.n, c0, c1, lane);
   const T wtot = warp_allreduce<T, OP>(acc);
-  if (lane == 0) s_warp[warp] = wtot;  // a warp without chunks exists only at the end of a row's last segment
+  if (lane == 0) s_warp[warp] = wtot;  // warps without chunks come last: their totals are never read
   __syncthreads();
 
   // Phase 2: publish the segment aggregate, gather the row's earlier ones.
   if (warp == 0) {
-    const T agg = block_scan_warp_totals<T, OP, NW>(s_warp, lane);
+    block_scan_warp_totals<T, OP, NW>(s_warp, lane);
+    __syncwarp();
+    const T agg = s_warp[nact - 1];
     if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
     if (part > 0) {
       bool timed_out;
@@ -395,7 +392,6 @@ cudaError_t launch_seg_op(const ScanJob& job, const LaunchCtx& ctx) {
   SegArgs<T> a;
   a.n = job.R;
   a.nc = p.nc;
-  a.warps = p.warps;
   a.segs = p.segs;
   a.ctas = p.ctas;
   a.counter = (unsigned*)job.temp;
@@ -527,7 +523,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<
   __syncthreads();
   const unsigned seg = s_seg;  // one row: the segment is its part
   long long c0, c1;
-  seg_chunks(a, seg, warp, NW, c0, c1);
+  const int nact = seg_chunks(a, seg, warp, NW, c0, c1);
 
   // Phase 1: lane totals of every chunk (kept), and the warp's total.
   const unsigned long long keep = l2_policy_evict_last();
@@ -546,12 +542,14 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<
     acc = c == c0 ? t : Op<T, OP>::f(acc, t);
   }
   const T wtot = warp_allreduce<T, OP>(acc);
-  if (lane == 0) s_warp[warp] = wtot;  // a warp without chunks exists only at the end of the last segment
+  if (lane == 0) s_warp[warp] = wtot;  // warps without chunks come last: their totals are never read
   __syncthreads();
 
   // Phase 2: as in scan_seg_kernel.
   if (warp == 0) {
-    const T agg = block_scan_warp_totals<T, OP, NW>(s_warp, lane);
+    block_scan_warp_totals<T, OP, NW>(s_warp, lane);
+    __syncwarp();
+    const T agg = s_warp[nact - 1];
     if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
     if (seg > 0) {
       bool timed_out;
@@ -622,7 +620,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<
 // The warps' lane totals live in G::MAXCPW shared-memory slots per warp, so a plan
 // whose warps take more chunks than that does not fit this geometry.
 template <class G> bool seg_chunk_plan_fits(const SegPlan& p) {
-  return p.warps > 0 && (p.nc + p.warps - 1) / p.warps <= G::MAXCPW;
+  return p.ctas > 0 && p.cpw <= G::MAXCPW;
 }
 
 template <class T, class G = SegChunkGeom<T>> bool seg_chunk_applies(const ScanJob& job, int num_sms) {
@@ -639,7 +637,6 @@ cudaError_t launch_seg_chunk_op(const ScanJob& job, const LaunchCtx& ctx) {
   SegArgs<T> a;
   a.n = job.R;
   a.nc = p.nc;
-  a.warps = p.warps;
   a.segs = p.segs;
   a.ctas = p.ctas;
   a.counter = (unsigned*)job.temp;

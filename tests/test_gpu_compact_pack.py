@@ -158,3 +158,45 @@ def test_pack_capacity_and_negative_counts():
     assert int(tot.item()) == w_total
     assert np.array_equal(offs.cpu().numpy().astype(np.int64), w_offs)
     assert np.array_equal(recs.cpu().numpy()[:w_total], w_recs[:w_total])
+
+
+@pytest.mark.parametrize("n", [511, 512, 513, 16_385, 2_490_368 + 1, 3_000_017])
+def test_pack_segment_sizes(n):
+    """Chunk (512 counts), CTA and warp-saturation boundaries of the segment kernel."""
+    check_pack(workloads.poisson_counts(n, 4.0, n % 991), "seg poisson n=%d" % n)
+    z = np.zeros(n, dtype=np.int32)
+    z[n // 3] = 1000   # one object owns many slots and blocks of slots
+    z[-1] = 3
+    check_pack(z, "seg sparse n=%d" % n)
+    assert gb.device_error() == gb.OK
+
+
+@pytest.mark.parametrize("n", [2, 4097, 100_003])
+def test_pack_unaligned_counts(n):
+    """Counts that are not 16-byte aligned take the tile kernel."""
+    k = workloads.poisson_counts(n + 1, 3.0, 5)
+    total = int(k[1:].astype(np.int64).sum())
+    offs, recs, tot = gb.pack_by_counts(dev(k)[1:], total)
+    w_offs, w_recs, w_total = oracle.pack_by_counts(k[1:], capacity=total)
+    assert int(tot.item()) == w_total
+    assert np.array_equal(offs.cpu().numpy().astype(np.int64), w_offs)
+    assert np.array_equal(recs.cpu().numpy()[:total], w_recs[:total])
+
+
+@pytest.mark.parametrize("aligned", [True, False])
+def test_pack_saturation(aligned):
+    """Offsets saturate at 2^31: exact below it, 2^31 - 1 from there on; the total is
+    reported as 2^31 - 1 with GB_ERR_RANGE, and records stop at the capacity."""
+    n = 100_000
+    k = np.zeros(n + 1, dtype=np.int32)
+    k[50_001] = 2**30
+    k[70_001] = 2**30
+    k[70_002] = 7
+    kd = dev(k)[1:] if not aligned else dev(k[1:])
+    offs, recs, tot = gb.pack_by_counts(kd, 1000)
+    w_offs, w_recs, w_total = oracle.pack_by_counts(k[1:], capacity=1000)
+    assert w_total == 2**31 + 7
+    assert int(tot.item()) == 2**31 - 1
+    assert np.array_equal(offs.cpu().numpy().astype(np.int64), np.minimum(w_offs, 2**31 - 1))
+    assert np.array_equal(recs.cpu().numpy()[:1000], w_recs[:1000])
+    assert gb.device_error() == gb.ERR_RANGE
