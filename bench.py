@@ -435,22 +435,24 @@ def our_arm(args, rank, world, local_rank):
     torch.cuda.synchronize()
     call_ms_events = float(np.mean([b.elapsed_time(a) for b, a in zip(k_before, k_after)]))
 
-    # End to end through the same C ABI: pinned host input -> device -> scan -> host.
+    # End to end through the C ABI's host-buffer scan: pinned host input -> device ->
+    # scan -> pinned host output, in chunks whose copies overlap the scans.
     xh = torch.from_numpy(x_host).pin_memory()
     yh = torch.empty_like(xh).pin_memory()
+    work = torch.empty(gb.host_scan_work_bytes(torch.float32, n), dtype=torch.uint8, device=device)
+    e2e_step = lambda: gb.scan_inclusive_host(xh, out=yh, work=work, stream=stream)  # noqa: E731
     e2e_steps = max(3, min(args.steps, 30))
-    for _ in range(2):
-        x.copy_(xh, non_blocking=True)
-        step()
-        yh.copy_(y, non_blocking=True)
+    for _ in range(3):
+        e2e_step()
     torch.cuda.synchronize()
+    a_h, a_d = yh[-1000:].numpy().astype(np.float64), y[-1000:].cpu().numpy().astype(np.float64)
+    if not np.all(np.abs(a_h - a_d) <= 1e-4 * (1.0 + np.abs(a_d))) or gb.device_error() != gb.OK:
+        raise RuntimeError("host-buffer scan disagrees with the device scan")  # different sum order: a tolerance
     barrier(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        x.copy_(xh, non_blocking=True)
-        step()
-        yh.copy_(y, non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, device)
@@ -507,7 +509,9 @@ def our_arm(args, rank, world, local_rank):
                      "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_src},
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": n * 4, "d2h_bytes_per_step": n * 4, "steps": e2e_steps,
-                "ms_per_step": round(e2e_ms, 3)},
+                "ms_per_step": round(e2e_ms, 3),
+                "call": "gb_scan_inclusive_host (pinned host buffers; 48 MiB chunks, copies in and out "
+                        "overlapping the scans)"},
         "gpu_launches": 2 * args.steps, "launches_per_step": {"status clear": 1, kname: 1},
         "clocks": clocks,
         "compaction_headline": None,

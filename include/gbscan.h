@@ -168,6 +168,44 @@ int gb_scan_reduce_then_scan(int dtype, int op, int inclusive, const void* in, v
                              void* stream);
 
 /*
+ * Inclusive scan of a HOST array into a host array (lanes = 1): the library copies
+ * the input to the device, scans it and copies the result back, chunk by chunk, so
+ * that the copy of one chunk in and of another out overlap the scan of a third
+ * (separate copy streams, a ring of three device buffers, events between them).
+ * Each chunk is scanned by the segment kernel starting from the running total of
+ * the chunks before it, which stays in device memory: the result is that of one
+ * inclusive scan of the whole array ([HB] 13.3.3's reduce-then-scan of a long
+ * array, piece by piece).  The pages have no counterpart: their host functions take
+ * device arrays.
+ *   dtype, op         as gb_scan_inclusive
+ *   in_host, out_host HOST pointers to n elements each, owned by the caller; pinned
+ *                     (cudaMallocHost / cudaHostRegister) for the copies to overlap,
+ *                     pageable memory works but copies synchronously; out_host may
+ *                     equal in_host; neither is touched after the work on `stream`
+ *                     completes
+ *   n                 element count (0: no-op)
+ *   chunk_elems       elements per chunk, 0 for the default (48 MiB of elements);
+ *                     capped at 48 MiB and rounded up to 16 bytes
+ *   work, work_bytes  device scratch of at least gb_host_scan_work_bytes(dtype, n,
+ *                     chunk_elems) bytes (256-byte aligned), or NULL: the library
+ *                     then allocates it on `stream` (cudaMallocAsync) and frees it
+ *                     there
+ *   stream            the caller's stream: the scans run on it, and it waits for the
+ *                     last chunk to be back in host memory, so synchronising it (or
+ *                     an event recorded on it after the call) means out_host is ready
+ * The copy streams and events are the library's, one set per device; calls on one
+ * device from several host threads are enqueued one after the other.  Floating-
+ * point results may differ from gb_scan_inclusive's in the last bits (the sum is
+ * combined in another order).  Errors: as gb_scan_inclusive; a failed CUDA call
+ * mid-way returns GB_ERR_CUDA with the chunks before it enqueued.
+ */
+int gb_scan_inclusive_host(int dtype, int op, const void* in_host, void* out_host, int64_t n,
+                           int64_t chunk_elems, void* work, size_t work_bytes, void* stream);
+
+/* Device scratch bytes for gb_scan_inclusive_host (0 for an invalid dtype or n <= 0). */
+size_t gb_host_scan_work_bytes(int dtype, int64_t n, int64_t chunk_elems);
+
+/*
  * Inclusive scan that allocates nothing, for callers that cannot call cudaMalloc or
  * cudaMallocAsync (code running under an allocator it does not own, or that must not
  * grow the process's device memory after start-up).  The pages have no counterpart:

@@ -46,6 +46,8 @@ SIGNATURES = {
     "gb_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "gb_set_stalled_tile": (None, [_i64]),
     "gb_scan_inclusive_noalloc": (_i, [_i, _i, _vp, _vp, _i64, _vp]),
+    "gb_scan_inclusive_host": (_i, [_i, _i, _vp, _vp, _i64, _i64, _vp, _sz, _vp]),
+    "gb_host_scan_work_bytes": (_sz, [_i, _i64, _i64]),
 }
 
 _lib = None
@@ -209,6 +211,33 @@ def pack_by_counts(counts, capacity: int, offsets: bool = True, out_records=None
                                     ctypes.c_void_p(out_total.data_ptr()), tp, tb, _stream(counts, stream)),
            "gb_pack_by_counts")
     return offs, out_records, out_total
+
+
+def scan_inclusive_host(x, op: str = "add", out=None, chunk_elems: int = 0, work=None, stream=None):
+    """Inclusive scan of a host (CPU) tensor into a host tensor through the device,
+    chunk by chunk with the copies overlapping the scans (pin both tensors for the
+    overlap).  Runs on `stream` (default: the current CUDA stream); synchronise it
+    before reading `out`."""
+    import torch
+    if x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous host tensor")
+    out = torch.empty_like(x, pin_memory=x.is_pinned()) if out is None else out
+    if out.is_cuda or not out.is_contiguous() or out.numel() != x.numel() or out.dtype != x.dtype:
+        raise ValueError("out must be a contiguous host tensor like x")
+    code, n = dtype_code(x.dtype), x.numel()
+    if work is not None:
+        wp, wb = ctypes.c_void_p(work.data_ptr()), work.numel() * work.element_size()
+    else:
+        wp, wb = None, 0
+    s = ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)) if stream is not None \
+        else ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    _check(load().gb_scan_inclusive_host(code, OPS[op], ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                         n, chunk_elems, wp, wb, s), "gb_scan_inclusive_host")
+    return out
+
+
+def host_scan_work_bytes(dtype, n: int, chunk_elems: int = 0) -> int:
+    return load().gb_host_scan_work_bytes(dtype_code(dtype), n, chunk_elems)
 
 
 def scan_reduce_then_scan(x, op: str = "add", inclusive: bool = True, init=None, out=None, temp=None,

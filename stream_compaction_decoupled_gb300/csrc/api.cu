@@ -198,9 +198,145 @@ int run_scan(int dtype, int op, int inclusive, const void* in, void* out, long l
   return GB_OK;
 }
 
+// ---- scans between host buffers: chunks whose copies overlap the scans --------------
+
+// Device copies of a host array move in chunks through a ring of kRing device buffers:
+// chunk i is copied in on one stream, scanned in place on the caller's stream (its
+// first element combined with the running total of chunks 0..i-1, which the previous
+// chunk's scan left in device memory), and copied out on another stream, so the copy
+// of chunk i+1 in and of chunk i-1 out run while chunk i is scanned.  Events order
+// each buffer's reuse.  The streams and events are made once per device.
+constexpr int kRing = 3;
+constexpr size_t kHostChunkBytes = 48ull << 20;  // a segment-kernel size (at most 96 MiB)
+
+struct HostPipe {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t in_done[kRing] = {}, scan_done[kRing] = {}, out_done[kRing] = {};
+  std::mutex mu;  // one call enqueues its chunks at a time on a device
+};
+HostPipe* g_pipe[kMaxDevices] = {};
+
+int get_pipe(HostPipe*& out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_pipe[dev]) {
+    HostPipe* p = new HostPipe();
+    const unsigned fl = cudaEventDisableTiming;
+    e = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->start, fl);
+    for (int k = 0; k < kRing && e == cudaSuccess; ++k) {
+      e = cudaEventCreateWithFlags(&p->in_done[k], fl);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->scan_done[k], fl);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->out_done[k], fl);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);  // the partly made pipe is leaked, not reused
+    g_pipe[dev] = p;
+  }
+  out = g_pipe[dev];
+  return GB_OK;
+}
+
+long long host_chunk_elems(int dtype, long long n, long long req) {
+  const long long es = (long long)dtype_size(dtype);
+  long long c = req > 0 ? req : (long long)(kHostChunkBytes / es);
+  if (c * es > (long long)kHostChunkBytes) c = (long long)(kHostChunkBytes / es);
+  c = (c + 15) / 16 * 16;  // whole 16-byte vectors (ring slots stay aligned)
+  return c < n ? c : n;
+}
+
+struct HostLayout {
+  size_t scan_temp = 0, carry = 0, slot = 0, total = 0;
+};
+HostLayout host_layout(int dtype, long long chunk) {
+  HostLayout L;
+  L.scan_temp = gbs::round_up(scan_temp(dtype, 1, chunk, 1), 256);
+  L.carry = 256;  // two carries
+  L.slot = gbs::round_up((size_t)chunk * dtype_size(dtype), 256);
+  L.total = L.scan_temp + L.carry + kRing * L.slot;
+  return L;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t gb_host_scan_work_bytes(int dtype, int64_t n, int64_t chunk_elems) {
+  if (!dtype_size(dtype) || n <= 0) return 0;
+  return host_layout(dtype, host_chunk_elems(dtype, n, chunk_elems)).total;
+}
+
+int gb_scan_inclusive_host(int dtype, int op, const void* in_host, void* out_host, int64_t n, int64_t chunk_elems,
+                           void* work, size_t work_bytes, void* stream) {
+  if (!dtype_size(dtype) || !valid_op(op) || n < 0 || chunk_elems < 0) return GB_ERR_INVALID;
+  if (n == 0) return GB_OK;
+  if (!in_host || !out_host) return GB_ERR_INVALID;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  ctx.ev_before = ctx.ev_after = nullptr;  // the profile hook times single-kernel calls only
+  HostPipe* pipe = nullptr;
+  rc = get_pipe(pipe);
+  if (rc) return rc;
+  const long long chunk = host_chunk_elems(dtype, n, chunk_elems);
+  const HostLayout L = host_layout(dtype, chunk);
+  Temp t;
+  rc = get_temp(work, work_bytes, L.total, ctx.stream, t);
+  if (rc) return rc;
+  char* base = (char*)t.p;
+  void* scan_tmp = base;
+  char* carry = base + L.scan_temp;
+  char* ring = carry + L.carry;
+  const size_t es = dtype_size(dtype);
+  const long long nchunks = (n + chunk - 1) / chunk;
+
+  std::lock_guard<std::mutex> lk(pipe->mu);
+  cudaError_t e = cudaEventRecord(pipe->start, ctx.stream);  // after the caller's earlier work
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(pipe->h2d, pipe->start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(pipe->d2h, pipe->start, 0);
+  for (long long i = 0; i < nchunks && e == cudaSuccess; ++i) {
+    const int k = (int)(i % kRing);
+    const long long off = i * chunk, len = n - off < chunk ? n - off : chunk;
+    const size_t bytes = (size_t)len * es;
+    char* buf = ring + (size_t)k * L.slot;
+    if (i >= kRing) e = cudaStreamWaitEvent(pipe->h2d, pipe->out_done[k], 0);  // slot copied out
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(buf, (const char*)in_host + (size_t)off * es, bytes, cudaMemcpyHostToDevice, pipe->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(pipe->in_done[k], pipe->h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx.stream, pipe->in_done[k], 0);
+    if (e == cudaSuccess) {
+      gbs::ScanJob job;
+      job.op = op;
+      job.inclusive = 1;
+      job.in = buf;
+      job.out = buf;
+      job.B = 1;
+      job.R = len;
+      job.C = 1;
+      job.temp = scan_tmp;
+      job.carry_in = i > 0 ? carry + ((i - 1) % 2) * 16 : nullptr;
+      job.carry_out = i + 1 < nchunks ? carry + (i % 2) * 16 : nullptr;
+      e = with_type(dtype, [&](auto* tp) {
+        using T = std::remove_pointer_t<decltype(tp)>;
+        return gbs::launch_scan<T>(job, ctx);
+      });
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(pipe->scan_done[k], ctx.stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(pipe->d2h, pipe->scan_done[k], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync((char*)out_host + (size_t)off * es, buf, bytes, cudaMemcpyDeviceToHost, pipe->d2h);
+    if (e == cudaSuccess) e = cudaEventRecord(pipe->out_done[k], pipe->d2h);
+  }
+  // The caller's stream resumes once the last chunk is back in host memory (copies
+  // leave each stream in order, so every earlier copy has finished too).
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx.stream, pipe->out_done[(nchunks - 1) % kRing], 0);
+  return e == cudaSuccess ? GB_OK : cuda_fail(e);
+}
+
+
 
 int gb_scan_inclusive(int dtype, int lanes, int op, const void* in, void* out, int64_t n, void* temp,
                       size_t temp_bytes, void* stream) {

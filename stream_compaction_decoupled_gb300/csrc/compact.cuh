@@ -188,19 +188,31 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
     const long long v1 = e1 / VEC;
     const uint4* p = reinterpret_cast<const uint4*>(a.in);
     long long v = c0 * CH / VEC + lane;
-    for (; v < v1; v += 32 * U) {  // U loads in flight, the last round guarded
+    for (; v + 32 * (U - 1) < v1; v += 32 * U) {  // U loads in flight
       uint4 u[U];
 #pragma unroll
-      for (int k = 0; k < U; ++k)
-        if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
+      for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
 #pragma unroll
       for (int k = 0; k < U; ++k) {
-        if (v + 32 * k >= v1) break;
         Vec<T> x;
         memcpy(x.v, &u[k], 16);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) cnt += selects(x.v[e], a.thr, a.predmask) ? 1u : 0u;
       }
+    }
+    if (v < v1) {  // the rest in one guarded round
+      uint4 u[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k)
+        if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
+#pragma unroll
+      for (int k = 0; k < U; ++k)
+        if (v + 32 * k < v1) {
+          Vec<T> x;
+          memcpy(x.v, &u[k], 16);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) cnt += selects(x.v[e], a.thr, a.predmask) ? 1u : 0u;
+        }
     }
     if (lane == 0)
       for (long long i = v1 * VEC; i < e1; ++i) cnt += selects(a.in[i], a.thr, a.predmask) ? 1u : 0u;

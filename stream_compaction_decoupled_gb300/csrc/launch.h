@@ -31,6 +31,11 @@ struct ScanJob {
   const void* init_host = nullptr;  // exclusive: init_lanes values (host); lane c uses c % init_lanes
   int init_lanes = 1;
   void* temp = nullptr;             // >= scan_temp_bytes<T>(B, R, C), 256-byte aligned
+  // One row, inclusive, segment kernels only: a device value combined on the left of
+  // every output (the total of earlier pieces of a longer array), and where the row's
+  // last output (its inclusive total, carry_in included) is copied.  Either may be null.
+  const void* carry_in = nullptr;
+  void* carry_out = nullptr;
 };
 
 struct CompactJob {

@@ -242,17 +242,25 @@ __global__ void __launch_bounds__(PackSegGeom::NT, PackSegGeom::MINB) pack_seg_k
     const uint4* p = reinterpret_cast<const uint4*>(a.counts);
     unsigned long long sum = 0;
     long long v = c0 * CH / VEC + lane;
-    for (; v < v1; v += 32 * U) {  // U loads in flight, the last round guarded
+    for (; v + 32 * (U - 1) < v1; v += 32 * U) {  // U loads in flight
+      uint4 u[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
+#pragma unroll
+      for (int k = 0; k < U; ++k)
+        sum += (unsigned long long)(unsigned)max((int)u[k].x, 0) + (unsigned)max((int)u[k].y, 0) +
+               (unsigned)max((int)u[k].z, 0) + (unsigned)max((int)u[k].w, 0);
+    }
+    if (v < v1) {  // the rest in one guarded round
       uint4 u[U];
 #pragma unroll
       for (int k = 0; k < U; ++k)
         if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
 #pragma unroll
-      for (int k = 0; k < U; ++k) {
-        if (v + 32 * k >= v1) break;
-        sum += (unsigned long long)(unsigned)max((int)u[k].x, 0) + (unsigned)max((int)u[k].y, 0) +
-               (unsigned)max((int)u[k].z, 0) + (unsigned)max((int)u[k].w, 0);
-      }
+      for (int k = 0; k < U; ++k)
+        if (v + 32 * k < v1)
+          sum += (unsigned long long)(unsigned)max((int)u[k].x, 0) + (unsigned)max((int)u[k].y, 0) +
+                 (unsigned)max((int)u[k].z, 0) + (unsigned)max((int)u[k].w, 0);
     }
     if (lane == 0)
       for (long long i = v1 * VEC; i < e1; ++i) sum += (unsigned)max(a.counts[i], 0);

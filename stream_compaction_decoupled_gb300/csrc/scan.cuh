@@ -25,6 +25,10 @@ template <class T> size_t scan_temp_bytes(long long B, long long R, long long C)
 }
 
 template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& ctx) {
+  if (job.carry_in || job.carry_out) {  // pieces of a longer row: the segment kernels, inclusive
+    const bool ok = std::is_same<T, double>::value ? seg_chunk_applies<T>(job, ctx.num_sms) : seg_applies<T>(job);
+    if (!ok || job.B != 1 || job.C != 1 || !job.inclusive) return cudaErrorInvalidValue;
+  }
   if constexpr (std::is_same<T, double>::value) {
     if (seg_chunk_applies<T>(job, ctx.num_sms)) {
       switch (job.op) {

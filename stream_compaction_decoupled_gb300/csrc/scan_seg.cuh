@@ -96,7 +96,27 @@ template <class T> struct SegArgs : SegArgsBase {
   T* out;
   T init;
   int inclusive;
+  const T* carry_in;  // nullable: combined on the left of everything (one row only)
+  T* carry_out;       // nullable: the row's last inclusive value (inclusive scans, one row)
 };
+
+// Phase 2's result for one segment, by lane 0 of warp 0: the base, carry-in on the
+// left of the gathered aggregates of the row's earlier segments.  (The row's total
+// for carry_out is taken from its last scanned element in phase 3: the aggregates
+// of a ragged last chunk hold the padding read past n.)
+template <class T, int OP>
+__device__ __forceinline__ void seg_finish_base(const SegArgs<T>& a, bool have_gather, T gathered, T& base,
+                                                bool& has) {
+  has = false;
+  if (a.carry_in) {
+    base = *a.carry_in;
+    has = true;
+  }
+  if (have_gather) {
+    base = has ? Op<T, OP>::f(base, gathered) : gathered;
+    has = true;
+  }
+}
 
 // Chunk loads and stores.  A full chunk moves as 16-byte vectors with an L2 policy;
 // the one ragged chunk at the end of the input moves element by element (elements
@@ -179,19 +199,31 @@ __device__ __forceinline__ T seg_reduce_part(const T* in, long long n, long long
     for (int e = 1; e < VEC; ++e) acc = Op<T, OP>::f(acc, x.v[e]);
     v += 32;
   }
-  for (; v < v1; v += 32 * U) {  // U loads in flight, the last round guarded
+  for (; v + 32 * (U - 1) < v1; v += 32 * U) {  // U loads in flight
     uint4 u[U];
 #pragma unroll
-    for (int k = 0; k < U; ++k)
-      if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
+    for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
 #pragma unroll
     for (int k = 0; k < U; ++k) {
-      if (v + 32 * k >= v1) break;
       Vec<T> x;
       memcpy(x.v, &u[k], 16);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) acc = Op<T, OP>::f(acc, x.v[e]);
     }
+  }
+  if (v < v1) {  // the rest in one guarded round, its loads still all in flight
+    uint4 u[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (v + 32 * k < v1) {
+        Vec<T> x;
+        memcpy(x.v, &u[k], 16);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc = Op<T, OP>::f(acc, x.v[e]);
+      }
   }
   if (lane == 0)
     for (long long i = v1 * VEC; i < e1; ++i) acc = Op<T, OP>::f(acc, in[i]);
@@ -273,6 +305,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, 
   __shared__ unsigned s_seg;
   __shared__ T s_warp[NW];
   __shared__ T s_base;
+  __shared__ int s_hbase;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
   __syncthreads();
@@ -295,19 +328,24 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, 
     __syncwarp();
     const T agg = s_warp[nact - 1];
     if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
+    T gathered{};
     if (part > 0) {
       bool timed_out;
-      const T base = seg_gather<T, OP, G::M>(st, seg - part, part, a.wait_ns, timed_out);
-      if (lane == 0) {
-        s_base = base;
-        if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
-      }
+      gathered = seg_gather<T, OP, G::M>(st, seg - part, part, a.wait_ns, timed_out);
+      if (lane == 0 && timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+    }
+    if (lane == 0) {
+      T b{};
+      bool h;
+      seg_finish_base<T, OP>(a, part > 0, gathered, b, h);
+      s_base = b;
+      s_hbase = h;
     }
   }
   __syncthreads();
 
   // Phase 3: rescan the warp's chunks from L2, seeded.
-  bool hb = part > 0;
+  bool hb = s_hbase != 0;
   T base = s_base;
   if (warp > 0) {
     const T wp = s_warp[warp - 1];
@@ -328,6 +366,16 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, 
     const T ctot = regs_reduce_pass<T, OP, ROUNDS>(x, lane, pre);
     regs_apply_pass<T, OP, ROUNDS>(x, lane, pre, base, hb, a.inclusive);
     seg_store<T, ROUNDS>(x, out, c * CH, a.n, lane, drop);
+    if (a.carry_out && c == a.nc - 1) {  // the row's last element: its inclusive value
+      constexpr int VEC = G::VEC;
+      const int el = (int)(a.n - 1 - c * CH);
+      T last = x[0].v[0];  // register selects: a runtime index would put x[] in local memory
+#pragma unroll
+      for (int j = 0; j < ROUNDS; ++j)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) last = ((j * 32 + lane) * VEC + e == el) ? x[j].v[e] : last;
+      if (lane == (el / VEC) % 32) *a.carry_out = last;
+    }
     base = hb ? Op<T, OP>::f(base, ctot) : ctot;
     hb = true;
 #pragma unroll
@@ -403,6 +451,8 @@ cudaError_t launch_seg_op(const ScanJob& job, const LaunchCtx& ctx) {
   a.init = T{};
   if (!job.inclusive && job.init_host) memcpy(&a.init, job.init_host, sizeof(T));
   a.inclusive = job.inclusive;
+  a.carry_in = (const T*)job.carry_in;
+  a.carry_out = (T*)job.carry_out;
   auto st = seg_status<T>(job.temp);
   profile_before(ctx);
   cudaError_t e = clear_status(job.temp, seg_reset_bytes<T>(), nullptr, 0, ctx);
@@ -516,6 +566,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<
   __shared__ unsigned s_seg;
   __shared__ T s_warp[NW];
   __shared__ T s_base;
+  __shared__ int s_hbase;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   T* s_tot = reinterpret_cast<T*>(seg_chunk_smem) + warp * MAXCPW * 32;  // [chunk][lane]
   T* s_stage = reinterpret_cast<T*>(seg_chunk_smem + G::TOT_BYTES) + warp * 32 * KH;
@@ -551,20 +602,25 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<
     __syncwarp();
     const T agg = s_warp[nact - 1];
     if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
+    T gathered{};
     if (seg > 0) {
       bool timed_out;
-      const T base = seg_gather<T, OP, G::M>(st, 0, seg, a.wait_ns, timed_out);
-      if (lane == 0) {
-        s_base = base;
-        if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
-      }
+      gathered = seg_gather<T, OP, G::M>(st, 0, seg, a.wait_ns, timed_out);
+      if (lane == 0 && timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+    }
+    if (lane == 0) {
+      T b{};
+      bool h;
+      seg_finish_base<T, OP>(a, seg > 0, gathered, b, h);
+      s_base = b;
+      s_hbase = h;
     }
   }
   __syncthreads();
 
   // Phase 3: per chunk, a warp scan of the kept lane totals seeds each lane's serial
   // scan of its own elements.
-  bool hb = seg > 0;
+  bool hb = s_hbase != 0;
   T base = s_base;
   if (warp > 0) {
     const T wp = s_warp[warp - 1];
@@ -611,6 +667,13 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<
         }
       }
       lane_store_staged<T, K>(x, s_stage, a.out, c * CH + hh * KH, a.n, lane, drop);
+      if (a.carry_out && c == a.nc - 1) {  // the row's last element: its inclusive value
+        const long long el = a.n - 1 - (e0 + hh * KH);
+        T last = x[0];  // register selects, as in scan_seg_kernel
+#pragma unroll
+        for (int k = 0; k < KH; ++k) last = (el == k) ? x[k] : last;
+        if (el >= 0 && el < KH) *a.carry_out = last;
+      }
     }
     base = hb ? Op<T, OP>::f(base, ctot) : ctot;
     hb = true;
@@ -648,6 +711,8 @@ cudaError_t launch_seg_chunk_op(const ScanJob& job, const LaunchCtx& ctx) {
   a.init = T{};
   if (!job.inclusive && job.init_host) memcpy(&a.init, job.init_host, sizeof(T));
   a.inclusive = job.inclusive;
+  a.carry_in = (const T*)job.carry_in;
+  a.carry_out = (T*)job.carry_out;
   auto st = seg_status<T>(job.temp);
   auto kern = scan_seg_chunk_kernel<T, OP, G, decltype(st)>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::SMEM);
