@@ -41,6 +41,18 @@ template <class T> __device__ __forceinline__ bool selects(T x, T t, unsigned ma
   return (mask & cls) != 0;
 }
 
+// The same predicates fixed at compile time (LT LE GT GE EQ NE, the order of the C
+// ABI's GB_LT..GB_NE): one comparison each.  A NaN x selects only under NE, as the
+// class mask above gives (unordered is in NE's mask only).
+template <int PRED, class T> __device__ __forceinline__ bool select_pred(T x, T t) {
+  if constexpr (PRED == 0) return x < t;
+  else if constexpr (PRED == 1) return x <= t;
+  else if constexpr (PRED == 2) return x > t;
+  else if constexpr (PRED == 3) return x >= t;
+  else if constexpr (PRED == 4) return x == t;
+  else return !(x == t);
+}
+
 template <class T>
 __global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_kernel(CompactArgs<T> a, PackedStatus<unsigned> st) {
   pdl_entry();
@@ -154,24 +166,25 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_ke
 // segment scan (scan_seg.cuh): count per warp part, publish segment counts and
 // gather the earlier ones, rescan from L2 and write the indices.  Within a round,
 // a lane's selected elements get consecutive output slots after those of the
-// lanes before it (one ballot per vector slot), so every store of a round lands in
-// one window of at most 32 x VEC indices.
+// lanes before it (one ballot per vector slot); the round's indices are staged in
+// shared memory and stored as one contiguous window.
 template <class T> struct CompactSegArgs : SegArgsBase {
   const T* in;
   T thr;
-  unsigned predmask;
   int* out_idx;
   int* out_count;
 };
 
-template <class T, class G>
+template <class T, int PRED, class G>
 __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegArgs<T> a, PackedStatus<unsigned> st) {
   pdl_entry();
   constexpr int NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, CH = G::CH;
   __shared__ unsigned s_seg;
   __shared__ unsigned s_warp[NW];
   __shared__ unsigned s_base;
+  __shared__ int s_stage_all[NW * 32 * VEC];  // a round's indices, per warp
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* s_stage = s_stage_all + warp * 32 * VEC;
   if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
   __syncthreads();
   const unsigned seg = s_seg;
@@ -197,7 +210,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
         Vec<T> x;
         memcpy(x.v, &u[k], 16);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) cnt += selects(x.v[e], a.thr, a.predmask) ? 1u : 0u;
+        for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], a.thr) ? 1u : 0u;
       }
     }
     if (v < v1) {  // the rest in one guarded round
@@ -211,11 +224,11 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
           Vec<T> x;
           memcpy(x.v, &u[k], 16);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) cnt += selects(x.v[e], a.thr, a.predmask) ? 1u : 0u;
+          for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], a.thr) ? 1u : 0u;
         }
     }
     if (lane == 0)
-      for (long long i = v1 * VEC; i < e1; ++i) cnt += selects(a.in[i], a.thr, a.predmask) ? 1u : 0u;
+      for (long long i = v1 * VEC; i < e1; ++i) cnt += select_pred<PRED>(a.in[i], a.thr) ? 1u : 0u;
   }
   cnt = __reduce_add_sync(0xffffffffu, cnt);
   if (lane == 0) s_warp[warp] = cnt;
@@ -240,32 +253,44 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
   }
   __syncthreads();
 
-  // Phase 3: rescan from L2 and write the selected indices.
+  // Phase 3: rescan from L2 and write the selected indices (positions fit 32 bits:
+  // compaction inputs hold fewer than 2^31 elements).
   unsigned off = s_base + (warp > 0 ? s_warp[warp - 1] : 0u);
   const unsigned long long drop = l2_policy_evict_first();
   const unsigned lt = lanemask_lt();
+  const unsigned n32 = (unsigned)a.n;
   Vec<T> x[ROUNDS];
   if (c0 < c1) seg_load<T, ROUNDS>(x, a.in, c0 * CH, a.n, lane, drop);
   for (long long c = c0; c < c1; ++c) {
     Vec<T> y[ROUNDS];  // the next chunk, requested before this one is processed
     if (c + 1 < c1) seg_load<T, ROUNDS>(y, a.in, (c + 1) * CH, a.n, lane, drop);
+    const unsigned cbase = (unsigned)(c * CH);
+    const bool full = cbase + CH <= n32;  // no element past n: no bound checks
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) {
-      const long long p0 = c * CH + (long long)(j * 32 + lane) * VEC;
+      const unsigned p0 = cbase + (unsigned)((j * 32 + lane) * VEC);
       unsigned sel = 0, before = 0, total = 0;
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const bool s = p0 + e < a.n && selects(x[j].v[e], a.thr, a.predmask);
+        const bool s = (full || p0 + e < n32) && select_pred<PRED>(x[j].v[e], a.thr);
         const unsigned bal = __ballot_sync(0xffffffffu, s);
         before += __popc(bal & lt);
         total += __popc(bal);
         sel |= (unsigned)s << e;
       }
-      int* dst = a.out_idx + off + before;
+      // Stage the round's indices at their ranks, then store the round's contiguous
+      // output window with consecutive lanes on consecutive slots (whole lines, not
+      // 4-byte pieces spread over 32 x VEC slots).
+      if (total != 0) {  // warp-uniform
+        __syncwarp();
+        unsigned r = before;
 #pragma unroll
-      for (int e = 0; e < VEC; ++e)
-        if ((sel >> e) & 1u) *dst++ = (int)(p0 + e);
-      off += total;
+        for (int e = 0; e < VEC; ++e)
+          if ((sel >> e) & 1u) s_stage[r++] = (int)(p0 + e);
+        __syncwarp();
+        for (unsigned k = lane; k < total; k += 32) a.out_idx[off + k] = s_stage[k];
+        off += total;
+      }
     }
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) x[j] = y[j];
@@ -282,7 +307,7 @@ template <class T> size_t compact_temp_bytes(long long n) {
   return rows > seg ? rows : seg;
 }
 
-template <class T> cudaError_t launch_compact_seg(const CompactJob& job, const LaunchCtx& ctx, unsigned predmask) {
+template <class T, int PRED> cudaError_t launch_compact_seg_p(const CompactJob& job, const LaunchCtx& ctx) {
   using G = SegGeom<T>;
   const SegPlan p = seg_plan<G>(1, job.n, ctx.num_sms);
   if (p.ctas == 0) return cudaSuccess;
@@ -297,21 +322,31 @@ template <class T> cudaError_t launch_compact_seg(const CompactJob& job, const L
   a.stalled = ctx.stalled_tile;
   a.in = (const T*)job.in;
   memcpy(&a.thr, job.threshold_host, sizeof(T));
-  a.predmask = predmask;
   a.out_idx = job.out_idx;
   a.out_count = job.out_count;
   PackedStatus<unsigned> st = seg_status<unsigned>(job.temp);
   profile_before(ctx);
   cudaError_t e = clear_status(job.temp, seg_reset_bytes<unsigned>(), nullptr, 0, ctx);
-  if (e == cudaSuccess) e = launch_pdl(compact_seg_kernel<T, G>, p.ctas, G::NT, 0, ctx.stream, a, st);
+  if (e == cudaSuccess) e = launch_pdl(compact_seg_kernel<T, PRED, G>, p.ctas, G::NT, 0, ctx.stream, a, st);
   profile_after(ctx);
   return e;
+}
+
+template <class T> cudaError_t launch_compact_seg(const CompactJob& job, const LaunchCtx& ctx) {
+  switch (job.pred) {
+    case 0: return launch_compact_seg_p<T, 0>(job, ctx);
+    case 1: return launch_compact_seg_p<T, 1>(job, ctx);
+    case 2: return launch_compact_seg_p<T, 2>(job, ctx);
+    case 3: return launch_compact_seg_p<T, 3>(job, ctx);
+    case 4: return launch_compact_seg_p<T, 4>(job, ctx);
+    default: return launch_compact_seg_p<T, 5>(job, ctx);
+  }
 }
 
 template <class T> cudaError_t launch_compact(const CompactJob& job, const LaunchCtx& ctx) {
   using G = RowsGeom<T>;
   static const unsigned masks[6] = {1u, 3u, 4u, 6u, 2u, 13u};  // LT LE GT GE EQ NE
-  if (compact_seg_applies<T>(job)) return launch_compact_seg<T>(job, ctx, masks[job.pred]);
+  if (compact_seg_applies<T>(job)) return launch_compact_seg<T>(job, ctx);
   CompactArgs<T> a;
   a.in = (const T*)job.in;
   a.n = job.n;
