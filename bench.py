@@ -67,6 +67,7 @@ KERNEL_SOURCES = {
     "compact_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "compact.cuh"),
     "scan_lanes_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh"),
     "pack_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "pack.cu"),
+    "pack_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "pack.cu"),
     "rts_scan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "rts.cuh"),
 }
 
