@@ -386,8 +386,9 @@ __global__ void __launch_bounds__(C::NT, 1) scan_stash_kernel(StashArgs<T> a, S 
       if (stid == 0) {
         int cmd = S_SCAN;
         for (;;) {
-          // Re-load (from L2) tiles of this group's runs that already have a prefix.
-          while (issued - scanned < (unsigned)NS && ient < sh.claimed && sh.q_pready[ient % QD]) {
+          // Re-load (from L2) tiles of this group's runs whose aggregate is out (their
+          // tiles are in L2 from then on); the prefix is needed only to scan them.
+          while (issued - scanned < (unsigned)NS && ient < sh.claimed && sh.q_aready[ient % QD]) {
             __threadfence_block();
             const unsigned e = ient % QD;
             const unsigned r = sh.q_run[e];
@@ -404,9 +405,17 @@ __global__ void __launch_bounds__(C::NT, 1) scan_stash_kernel(StashArgs<T> a, S 
               itile = 0;
             }
           }
-          if (scanned < issued) break;
-          auto pready = [&] { return ient < sh.claimed && sh.q_pready[ient % QD] != 0; };
-          const bool got = stash_wait([&] { return pready() || (sh.i_finished && ient >= sh.claimed); },
+          if (scanned < issued) {
+            // The next tile to scan is loading; its run's prefix must be known.
+            if (!stash_wait([&] { return sh.q_pready[sent % QD] != 0; }, a.wait_ns, &sh.abort)) {
+              cmd = S_EXIT_ERR;
+              fail();
+            }
+            __threadfence_block();
+            break;
+          }
+          auto aready = [&] { return ient < sh.claimed && sh.q_aready[ient % QD] != 0; };
+          const bool got = stash_wait([&] { return aready() || (sh.i_finished && ient >= sh.claimed); },
                                       a.wait_ns, &sh.abort);
           __threadfence_block();
           if (!got) {
@@ -414,7 +423,7 @@ __global__ void __launch_bounds__(C::NT, 1) scan_stash_kernel(StashArgs<T> a, S 
             fail();
             break;
           }
-          if (pready()) continue;
+          if (aready()) continue;
           cmd = S_EXIT;
           break;
         }
