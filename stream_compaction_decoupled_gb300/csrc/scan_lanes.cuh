@@ -42,10 +42,14 @@ template <class T> struct LanesArgs {
 // and 1e6x8 axis 0, 96-byte structs, 17-lane duals, 1000x1e4 fp64 axis 0) put 32 at
 // or near the best everywhere: fewer, larger tiles mean fewer look-backs along a
 // chain, which is what limits these scans (dual16 1e6: 372 us at 8, 165 us at 32).
-template <class T, int RPG_ = 32> struct LanesGeomT {
+template <class T, int RPG_ = 32, int D_ = 4> struct LanesGeomT {
   static constexpr int NT = 256;
   static constexpr int NW = NT / 32;
   static constexpr int RPG = RPG_;                        // rows per thread
+  // Look-back: predecessors per round trip of a lane's thread.  4 is best on every
+  // lane workload measured (96-byte structs 1e6: 51.9 / 59.5 / 62.1 us at 4 / 8 / 16;
+  // 17-lane duals 1e6: 162 / 176 / 232 us): wider windows cost registers and occupancy.
+  static constexpr int D = D_;
   static constexpr int CTMAX = sizeof(T) == 4 ? 64 : 32;  // 256-byte strips
   static int ct(long long C) { return C <= CTMAX ? (int)C : CTMAX; }
   static int groups(int CT) {
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(Gm::NT) scan_lanes_kernel(LanesArgs<T> a, S st
     } else {
       if (!stalled) st.publish(si, FLAG_A, agg);
       bool timed_out;
-      const T pfx = lookback_lane<T, OP, 4>(st, first, tt, tid, CT, a.wait_ns, timed_out);
+      const T pfx = lookback_lane<T, OP, Gm::D>(st, first, tt, tid, CT, a.wait_ns, timed_out);
       if (!stalled) st.publish(si, FLAG_P, Op<T, OP>::f(pfx, agg));
       s_pfx[tid] = pfx;
       if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
