@@ -2,10 +2,12 @@
 // array.  C == 1 (contiguous rows): one row, or a few long rows, that fit in L2 go
 // to the segment kernel (fp64: its thread-contiguous variant, one row), one row many
 // times larger than L2 to the L2-resident look-back kernel, everything else to the
-// row kernel.  C > 1 (lanes / columns): the lane kernel.
+// row kernel.  C > 1 (lanes / columns): the lane look-back kernel, or for 8-byte lanes
+// in a few long chains that fit in L2, reduce-then-scan.
 #pragma once
 
 #include "scan_lanes.cuh"
+#include "scan_lanes_rts.cuh"
 #include "scan_rows.cuh"
 #include "scan_seg.cuh"
 #include "scan_stash.cuh"
@@ -21,6 +23,7 @@ template <class T> size_t scan_temp_bytes(long long B, long long R, long long C)
     const size_t m = rows > stash ? rows : stash;
     return m > seg ? m : seg;
   }
+  if (lanes_rts_applies<T>(B, R, C)) return lanes_rts_temp_bytes<T>(B, R, C);
   return lanes_temp_bytes<T>(B, R, C);
 }
 
@@ -57,6 +60,15 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
       case OP_ADD: return launch_rows_op<T, OP_ADD>(job, ctx);
       case OP_MAX: return launch_rows_op<T, OP_MAX>(job, ctx);
       default: return launch_rows_op<T, OP_MIN>(job, ctx);
+    }
+  }
+  if constexpr (sizeof(T) == 8) {
+    if (lanes_rts_applies<T>(job.B, job.R, job.C)) {
+      switch (job.op) {
+        case OP_ADD: return launch_lanes_rts_op<T, OP_ADD>(job, ctx);
+        case OP_MAX: return launch_lanes_rts_op<T, OP_MAX>(job, ctx);
+        default: return launch_lanes_rts_op<T, OP_MIN>(job, ctx);
+      }
     }
   }
   switch (job.op) {

@@ -146,16 +146,38 @@ __global__ void __launch_bounds__(Gm::NT) scan_lanes_kernel(LanesArgs<T> a, S st
   }
   __syncthreads();
 
-  // Exclusive scan of the group totals of each lane, one warp per lane.
+  // Exclusive scan of the group totals of each lane.  fp64: one thread per lane,
+  // serially (G - 1 adds a lane, where a warp-wide scan costs 5 x 32: fp64 adds are
+  // what bounds 8-byte float lanes on this GPU); else one warp per lane.
   const int ngroups = (rows + RPG - 1) / RPG;
-  for (int cc = warp; cc < cols; cc += NW) {
-    const T v = s_gx[(lane < ngroups ? lane : ngroups - 1) * CT + cc];
-    const T inc = warp_inclusive<T, OP>(v, lane);
-    const T exc = __shfl_up_sync(0xffffffffu, inc, 1);
-    const T agg = __shfl_sync(0xffffffffu, inc, ngroups - 1);
-    __syncwarp();
-    if (lane < ngroups && lane > 0) s_gx[lane * CT + cc] = exc;
-    if (lane == 0) s_pfx[cc] = agg;
+  if constexpr (std::is_same<T, double>::value) {
+    if (tid < cols) {
+      T run = s_gx[tid];
+      for (int g0 = 1; g0 < ngroups; g0 += 8) {
+        T v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (g0 + u < ngroups) v[u] = s_gx[(g0 + u) * CT + tid];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (g0 + u < ngroups) {
+            s_gx[(g0 + u) * CT + tid] = run;
+            run = Op<T, OP>::f(run, v[u]);
+          }
+        }
+      }
+      s_pfx[tid] = run;
+    }
+  } else {
+    for (int cc = warp; cc < cols; cc += NW) {
+      const T v = s_gx[(lane < ngroups ? lane : ngroups - 1) * CT + cc];
+      const T inc = warp_inclusive<T, OP>(v, lane);
+      const T exc = __shfl_up_sync(0xffffffffu, inc, 1);
+      const T agg = __shfl_sync(0xffffffffu, inc, ngroups - 1);
+      __syncwarp();
+      if (lane < ngroups && lane > 0) s_gx[lane * CT + cc] = exc;
+      if (lane == 0) s_pfx[cc] = agg;
+    }
   }
   __syncthreads();
 

@@ -121,7 +121,8 @@ def test_lane_vectors_along_rows(lanes):
 
 # ---- lane-vector scans over many tiles: one tile, several waves of tiles, ragged last
 # tiles, batches, 16-byte and odd row widths (tiles hold 320 rows of 24 fp32 lanes, 1024
-# rows of 8, 480 rows of 17 fp64 lanes).
+# rows of 8, 480 rows of 17 fp64 lanes).  8-byte lanes in a long single chain here take
+# reduce-then-scan, the rest the look-back lane kernel.
 
 LANE_SHAPES = [(1, 320, 24), (1, 321, 24), (1, 200_000, 24), (3, 100_003, 24), (1, 1_000_000, 8),
                (2, 4097, 8), (1, 300_000, 17), (5, 20_000, 17), (1, 150_000, 32), (1, 40_000, 64),
@@ -140,6 +141,42 @@ def test_lane_tiles(dt, op, shape):
     init = (np.arange(lanes) - 3).astype(NP[dt]) if op == "add" else x[:lanes].copy()
     got = gb.scan_batched(xd, axis=1, op=op, inclusive=False, init=init, lanes=lanes).cpu().numpy()
     assert_scan_matches(got, as3(x, b, n, lanes), op, False, init, what="lanes excl %s" % (shape,))
+    assert gb.device_error() == gb.OK
+
+
+# 8-byte lanes in at most 4 chains of at least 128 look-back tiles, in at most 160 MiB,
+# take reduce-then-scan: whole rows (1 and 3 batches), 64-lane strips (2 strips x 2
+# batches), an 8-lane last strip, a 1-lane last strip (plain loads), 2 lanes (1024-row
+# tiles), and each through a view one element off 16-byte alignment (plain loads).
+RTS_SHAPES = [(1, 300_000, 17), (2, 70_000, 64), (1, 130_000, 40), (1, 130_000, 33), (1, 300_000, 2),
+              (3, 130_000, 17)]
+
+
+@pytest.mark.parametrize("dt", ["f64", "i64"])
+@pytest.mark.parametrize("op", ["add", "max"])
+@pytest.mark.parametrize("shape", RTS_SHAPES)
+@pytest.mark.parametrize("offset", [0, 1])
+def test_rts_lanes(dt, op, shape, offset):
+    b, n, lanes = shape
+    x = make(dt, b * n * lanes + offset, b * n + lanes + offset)
+    xd = dev(x)[offset:].reshape(b, n, lanes)
+    x = x[offset:]
+    got = gb.scan_batched(xd, axis=1, op=op, lanes=lanes).cpu().numpy()
+    assert_scan_matches(got, as3(x, b, n, lanes), op, True, what="rts %s %s %s +%d" % (dt, op, shape, offset))
+    init = (np.arange(lanes) - 3).astype(NP[dt]) if op == "add" else x[:lanes].copy()
+    got = gb.scan_batched(xd, axis=1, op=op, inclusive=False, init=init, lanes=lanes).cpu().numpy()
+    assert_scan_matches(got, as3(x, b, n, lanes), op, False, init, what="rts excl %s +%d" % (shape, offset))
+    assert gb.device_error() == gb.OK
+
+
+# Above 160 MiB, 8-byte lanes in one long chain take the look-back lane kernel again.
+@pytest.mark.parametrize("op", ["add", "min"])
+@pytest.mark.parametrize("dt", ["f64", "i64"])
+def test_lane_kernel_long_chain_above_rts_limit(dt, op):
+    b, n, lanes = 1, 1_250_000, 17
+    x = make(dt, b * n * lanes, 77)
+    got = gb.scan_batched(dev(x).reshape(b, n, lanes), axis=1, op=op, lanes=lanes).cpu().numpy()
+    assert_scan_matches(got, as3(x, b, n, lanes), op, True, what="look-back lanes %s %s" % (dt, op))
     assert gb.device_error() == gb.OK
 
 
