@@ -69,6 +69,9 @@ KERNEL_SOURCES = {
     "pack_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "pack.cu"),
     "pack_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "pack.cu"),
     "rts_scan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "rts.cuh"),
+    "lanes_rts_reduce_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
+    "lanes_rts_spine_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
+    "lanes_rts_scan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
 }
 
 
