@@ -60,11 +60,17 @@ extern "C" {
 enum gb_dtype { GB_I32 = 0, GB_U32 = 1, GB_I64 = 2, GB_U64 = 3, GB_F32 = 4, GB_F64 = 5 };
 
 /* Associative operators ([PS] "Exclusive Prefix Sum": an operator (+) with an
- * identity I; "Other Applications": max for visibility).  ADD wraps modulo 2^32 /
- * 2^64 for integers.  MAX / MIN on floats follow fmax / fmin (a NaN operand is
- * ignored).  MAX and MIN are treated as operators WITHOUT a neutral element
- * ([AK]): inclusive scans need none, exclusive scans need `init`. */
-enum gb_op { GB_ADD = 0, GB_MAX = 1, GB_MIN = 2 };
+ * identity I; "Other Applications": max for visibility; [AK]: the accumulate API's
+ * cumsum and cumprod).  ADD and MUL wrap modulo 2^32 / 2^64 for integers (the low
+ * bits of the exact sum or product, two's complement).  MAX / MIN on floats follow
+ * fmax / fmin (a NaN operand is ignored).  MAX and MIN are treated as operators
+ * WITHOUT a neutral element ([AK]): inclusive scans need none, exclusive scans need
+ * `init`.  ADD's neutral element is 0, MUL's 1.  Float ADD and MUL round in the
+ * element type; results are compared against exact (fp64) prefixes within the
+ * rounding bounds of any bracketing: sums within 1e-5 of the prefix sum of |x|,
+ * products within a relative (i + 1) u / (1 - (i + 1) u) at position i (u the
+ * unit roundoff of the type). */
+enum gb_op { GB_ADD = 0, GB_MAX = 1, GB_MIN = 2, GB_MUL = 3 };
 
 /* Compaction predicates: element x is selected when  x <op> threshold. */
 enum gb_pred { GB_LT = 0, GB_LE = 1, GB_GT = 2, GB_GE = 3, GB_EQ = 4, GB_NE = 5 };
@@ -106,8 +112,8 @@ int gb_scan_inclusive(int dtype, int lanes, int op, const void* in, void* out, i
  * Exclusive scan  e_i = init (+) a_0 (+) ... (+) a_{i-1}  ([PS] "Exclusive Prefix
  * Sum"; the caller's init takes the place of the identity I and is folded in on
  * the left of every output).  `init` is a host pointer to one element (lanes
- * values) or NULL: NULL means 0 for GB_ADD and is refused for MAX / MIN with
- * GB_ERR_NO_IDENTITY.  The exclusive value is the prefix of the predecessors (a
+ * values) or NULL: NULL means 0 for GB_ADD and 1 for GB_MUL, and is refused for
+ * MAX / MIN with GB_ERR_NO_IDENTITY.  The exclusive value is the prefix of the predecessors (a
  * shift), not inclusive minus x ([HB] 13.3.1 derives it by subtraction, which
  * holds for add only).
  */

@@ -26,7 +26,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _DTYPES = {"i32": 0, "u32": 1, "i64": 2, "u64": 3, "f32": 4, "f64": 5}
 _NP = {"i32": np.int32, "u32": np.uint32, "i64": np.int64, "u64": np.uint64,
        "f32": np.float32, "f64": np.float64}
-_OPS = {"add": 0, "max": 1, "min": 2}
+_OPS = {"add": 0, "max": 1, "min": 2, "mul": 3}
 _PREDS = {"lt": 0, "le": 1, "gt": 2, "ge": 3, "eq": 4, "ne": 5}
 
 _lib = None
@@ -71,8 +71,8 @@ class NoIdentity(ValueError):
 def scan3(x: np.ndarray, op: str = "add", inclusive: bool = True, init=None) -> np.ndarray:
     """Scan a (B, R, C) array along axis 1 (the middle axis).
 
-    Integer inputs give the same integer type (wrapping add); float inputs give
-    fp64.  ``init`` (exclusive only) is a scalar or a sequence of lane values;
+    Integer inputs give the same integer type (wrapping add and multiply); float
+    inputs give fp64.  ``init`` (exclusive only) is a scalar or a sequence of lane values;
     lane c starts from init[c % len(init)].
     """
     x = np.ascontiguousarray(x)

@@ -12,13 +12,18 @@
  *     inclusive  s_i = a_0 (+) a_1 (+) ... (+) a_i
  *     exclusive  e_0 = I,  e_i = a_0 (+) ... (+) a_{i-1}
  * Both are computed here as one left-to-right loop per scanned line, exactly
- * as written.  Readings where the pages leave a step open:
+ * as written.  The operators are add, max, min and multiply (the cumulative
+ * product that AcceleratedKernels.jl's accumulate API offers as cumprod).
+ * Readings where the pages leave a step open:
  *   - exclusive scans take a caller value `init` in place of I and fold it in
  *     on the left of every output (e_i = init (+) a_0 (+) ... (+) a_{i-1});
- *     for add a missing init means 0; max and min have no neutral element
- *     here, so an exclusive max/min without init is refused (return -2);
- *   - 32- and 64-bit integer add wraps modulo 2^32 / 2^64 (two's complement);
- *   - fp32 and fp64 add accumulate in fp64 and return fp64 (the fp64 oracle);
+ *     a missing init means 0 for add and 1 for multiply; max and min have no
+ *     neutral element here, so an exclusive max/min without init is refused
+ *     (return -2);
+ *   - 32- and 64-bit integer add and multiply wrap modulo 2^32 / 2^64 (two's
+ *     complement: the low bits of the exact result);
+ *   - fp32 and fp64 add and multiply accumulate in fp64 and return fp64 (the
+ *     fp64 oracle);
  *   - fp max/min follow C's fmax/fmin: a NaN operand is ignored;
  *   - a (B, R, C) row-major array is scanned along its middle axis: B
  *     independent batches, R scanned positions, C independent lanes.  A 1-D
@@ -43,7 +48,7 @@
  * in oracle/__init__.py (its own table; nothing here is shared with the GPU
  * library). */
 enum { OR_I32 = 0, OR_U32 = 1, OR_I64 = 2, OR_U64 = 3, OR_F32 = 4, OR_F64 = 5 };
-enum { OR_ADD = 0, OR_MAX = 1, OR_MIN = 2 };
+enum { OR_ADD = 0, OR_MAX = 1, OR_MIN = 2, OR_MUL = 3 };
 enum { OR_LT = 0, OR_LE = 1, OR_GT = 2, OR_GE = 3, OR_EQ = 4, OR_NE = 5 };
 
 #define OR_OK 0
@@ -56,6 +61,7 @@ static uint32_t op_u32bits_signed(int op, uint32_t acc, uint32_t x)
 {
     int32_t a = (int32_t)acc, b = (int32_t)x;
     if (op == OR_ADD) return acc + x; /* modulo 2^32 */
+    if (op == OR_MUL) return acc * x; /* the low 32 bits of the product */
     if (op == OR_MAX) return (uint32_t)(a > b ? a : b);
     return (uint32_t)(a < b ? a : b);
 }
@@ -63,6 +69,7 @@ static uint32_t op_u32bits_signed(int op, uint32_t acc, uint32_t x)
 static uint32_t op_u32bits_unsigned(int op, uint32_t acc, uint32_t x)
 {
     if (op == OR_ADD) return acc + x;
+    if (op == OR_MUL) return acc * x;
     if (op == OR_MAX) return acc > x ? acc : x;
     return acc < x ? acc : x;
 }
@@ -71,6 +78,7 @@ static uint64_t op_u64bits_signed(int op, uint64_t acc, uint64_t x)
 {
     int64_t a = (int64_t)acc, b = (int64_t)x;
     if (op == OR_ADD) return acc + x; /* modulo 2^64 */
+    if (op == OR_MUL) return acc * x; /* the low 64 bits of the product */
     if (op == OR_MAX) return (uint64_t)(a > b ? a : b);
     return (uint64_t)(a < b ? a : b);
 }
@@ -78,6 +86,7 @@ static uint64_t op_u64bits_signed(int op, uint64_t acc, uint64_t x)
 static uint64_t op_u64bits_unsigned(int op, uint64_t acc, uint64_t x)
 {
     if (op == OR_ADD) return acc + x;
+    if (op == OR_MUL) return acc * x;
     if (op == OR_MAX) return acc > x ? acc : x;
     return acc < x ? acc : x;
 }
@@ -85,6 +94,7 @@ static uint64_t op_u64bits_unsigned(int op, uint64_t acc, uint64_t x)
 static double op_f64(int op, double acc, double x)
 {
     if (op == OR_ADD) return acc + x;
+    if (op == OR_MUL) return acc * x;
     if (op == OR_MAX) return fmax(acc, x);
     return fmin(acc, x);
 }
@@ -103,7 +113,7 @@ static void scan_32(int is_signed, int op, int inclusive, const uint32_t *in,
 {
     for (int64_t b = 0; b < B; b++)
         for (int64_t c = 0; c < C; c++) {
-            uint32_t acc = 0;
+            uint32_t acc = op == OR_MUL ? 1u : 0u;
             if (!inclusive && init) acc = init[c % init_len];
             for (int64_t r = 0; r < R; r++) {
                 uint32_t x = in[at(b, r, c, R, C)];
@@ -127,7 +137,7 @@ static void scan_64(int is_signed, int op, int inclusive, const uint64_t *in,
 {
     for (int64_t b = 0; b < B; b++)
         for (int64_t c = 0; c < C; c++) {
-            uint64_t acc = 0;
+            uint64_t acc = op == OR_MUL ? 1u : 0u;
             if (!inclusive && init) acc = init[c % init_len];
             for (int64_t r = 0; r < R; r++) {
                 uint64_t x = in[at(b, r, c, R, C)];
@@ -153,7 +163,7 @@ static void scan_fp(int is_f32, int op, int inclusive, const void *in,
 {
     for (int64_t b = 0; b < B; b++)
         for (int64_t c = 0; c < C; c++) {
-            double acc = 0.0;
+            double acc = op == OR_MUL ? 1.0 : 0.0;
             if (!inclusive && init)
                 acc = is_f32 ? (double)((const float *)init)[c % init_len]
                              : ((const double *)init)[c % init_len];
@@ -185,9 +195,9 @@ int oracle_scan(int dtype, int op, int inclusive, const void *in, void *out,
                 int64_t init_len)
 {
     if (B < 0 || R < 0 || C < 0) return OR_BAD_ARGUMENT;
-    if (op != OR_ADD && op != OR_MAX && op != OR_MIN) return OR_BAD_ARGUMENT;
+    if (op != OR_ADD && op != OR_MAX && op != OR_MIN && op != OR_MUL) return OR_BAD_ARGUMENT;
     if (init && init_len < 1) return OR_BAD_ARGUMENT;
-    if (!inclusive && op != OR_ADD && !init) return OR_NO_IDENTITY;
+    if (!inclusive && (op == OR_MAX || op == OR_MIN) && !init) return OR_NO_IDENTITY;
     if (B == 0 || R == 0 || C == 0) return OR_OK;
     switch (dtype) {
     case OR_I32: scan_32(1, op, inclusive, in, out, B, R, C, init, init_len); break;

@@ -19,12 +19,12 @@ LIB_PATH = os.path.join(_HERE, "libgbscan.so")
 
 # Mirrors of the enums in include/gbscan.h.
 I32, U32, I64, U64, F32, F64 = range(6)
-ADD, MAX, MIN = range(3)
+ADD, MAX, MIN, MUL = range(4)
 LT, LE, GT, GE, EQ, NE = range(6)
 KIND_SCAN, KIND_BATCHED_AXIS1, KIND_BATCHED_AXIS0, KIND_COMPACT, KIND_PACK, KIND_REDUCE_THEN_SCAN = range(6)
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_TEMP, ERR_NO_IDENTITY, ERR_RANGE, ERR_CUDA, ERR_TIMEOUT = range(8)
 
-OPS = {"add": ADD, "max": MAX, "min": MIN}
+OPS = {"add": ADD, "max": MAX, "min": MIN, "mul": MUL}
 PREDS = {"lt": LT, "le": LE, "gt": GT, "ge": GE, "eq": EQ, "ne": NE}
 _NP_OF = {I32: np.int32, U32: np.uint32, I64: np.int64, U64: np.uint64, F32: np.float32, F64: np.float64}
 

@@ -2,6 +2,7 @@
 // (temp) handling, element-type dispatch and the sticky device error word.
 // Every check that can fail does so before anything is enqueued.
 #include <atomic>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 #include <vector>
@@ -124,7 +125,8 @@ size_t dtype_size(int dtype) {
   }
 }
 
-bool valid_op(int op) { return op == GB_ADD || op == GB_MAX || op == GB_MIN; }
+bool valid_op(int op) { return op == GB_ADD || op == GB_MAX || op == GB_MIN || op == GB_MUL; }
+bool has_identity(int op) { return op == GB_ADD || op == GB_MUL; }
 
 // Calls f.template operator()<T>() with T the C++ type of `dtype`.
 template <class F> auto with_type(int dtype, F&& f) {
@@ -136,6 +138,21 @@ template <class F> auto with_type(int dtype, F&& f) {
     case GB_F32: return f((float*)nullptr);
     default: return f((double*)nullptr);
   }
+}
+
+// The neutral element of ADD (0) or MUL (1), `lanes` copies in the element type.
+std::vector<unsigned char> identity_bytes(int dtype, int op, int lanes) {
+  const size_t es = dtype_size(dtype);
+  std::vector<unsigned char> v((size_t)lanes * es, 0);
+  if (op == GB_MUL) {
+    with_type(dtype, [&](auto* tp) {
+      using T = std::remove_pointer_t<decltype(tp)>;
+      const T one = T(1);
+      for (int l = 0; l < lanes; ++l) std::memcpy(v.data() + (size_t)l * es, &one, es);
+      return 0;
+    });
+  }
+  return v;
 }
 
 // Tiles are claimed with a 32-bit counter and indexed with grid.x.
@@ -163,7 +180,7 @@ int run_scan(int dtype, int op, int inclusive, const void* in, void* out, long l
              long long C, const void* init, int lanes, void* temp, size_t temp_bytes, void* stream) {
   if (!dtype_size(dtype) || !valid_op(op)) return GB_ERR_INVALID;
   if (lanes < 1 || lanes > kMaxLanes || B < 0 || R < 0 || C < 0) return GB_ERR_INVALID;
-  if (!inclusive && !init && op != GB_ADD) return GB_ERR_NO_IDENTITY;
+  if (!inclusive && !init && !has_identity(op)) return GB_ERR_NO_IDENTITY;
   if (B == 0 || R == 0 || C == 0) return GB_OK;
   if (!in || !out) return GB_ERR_INVALID;
   if ((long double)B * R * C > 9.0e18L) return GB_ERR_RANGE;
@@ -174,10 +191,10 @@ int run_scan(int dtype, int op, int inclusive, const void* in, void* out, long l
   Temp t;
   rc = get_temp(temp, temp_bytes, scan_temp(dtype, B, R, C), ctx.stream, t);
   if (rc) return rc;
-  std::vector<unsigned char> zeros;
-  if (!inclusive && !init) {  // add without init: start from 0
-    zeros.assign((size_t)lanes * dtype_size(dtype), 0);
-    init = zeros.data();
+  std::vector<unsigned char> neutral;
+  if (!inclusive && !init) {  // add / multiply without init: start from 0 / 1
+    neutral = identity_bytes(dtype, op, lanes);
+    init = neutral.data();
   }
   gbs::ScanJob job;
   job.op = op;
@@ -428,7 +445,7 @@ int gb_pack_by_counts(const int32_t* counts, int64_t n, int32_t* offsets, int32_
 int gb_scan_reduce_then_scan(int dtype, int op, int inclusive, const void* in, void* out, int64_t n,
                              const void* init, void* temp, size_t temp_bytes, void* stream) {
   if (!dtype_size(dtype) || !valid_op(op) || n < 0) return GB_ERR_INVALID;
-  if (!inclusive && !init && op != GB_ADD) return GB_ERR_NO_IDENTITY;
+  if (!inclusive && !init && !has_identity(op)) return GB_ERR_NO_IDENTITY;
   if (n == 0) return GB_OK;
   if (!in || !out) return GB_ERR_INVALID;
   LaunchCtx ctx;
@@ -441,14 +458,14 @@ int gb_scan_reduce_then_scan(int dtype, int op, int inclusive, const void* in, v
   Temp t;
   rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
   if (rc) return rc;
-  unsigned long long zero = 0;
+  const std::vector<unsigned char> neutral = identity_bytes(dtype, op, 1);
   gbs::RtsJob job;
   job.op = op;
   job.inclusive = inclusive ? 1 : 0;
   job.in = in;
   job.out = out;
   job.n = n;
-  job.init_host = init ? init : &zero;
+  job.init_host = init ? init : neutral.data();
   job.temp = t.p;
   const cudaError_t e = with_type(dtype, [&](auto* tp) {
     using T = std::remove_pointer_t<decltype(tp)>;

@@ -20,9 +20,10 @@ enum : unsigned { FLAG_X = 0, FLAG_A = 1, FLAG_P = 2 };
 // Bits of the sticky device error word.
 enum : unsigned { ERRBIT_TIMEOUT = 1u, ERRBIT_RANGE = 2u, ERRBIT_INVALID = 4u };
 
-// Operators.  OP_SATADD is internal to packing: unsigned add saturating at 2^31,
-// which keeps record offsets from wrapping while staying associative.
-enum { OP_ADD = 0, OP_MAX = 1, OP_MIN = 2, OP_SATADD = 3 };
+// Operators (the public gb_op values, plus OP_SATADD, internal to packing: unsigned
+// add saturating at 2^31, which keeps record offsets from wrapping while staying
+// associative).
+enum { OP_ADD = 0, OP_MAX = 1, OP_MIN = 2, OP_MUL = 3, OP_SATADD = 16 };
 
 // Op<T, OP>::f(a, b) = a (+) b, with `a` the earlier operand in scan order.
 template <class T, int OP> struct Op;
@@ -34,6 +35,16 @@ template <class T> struct Op<T, OP_ADD> {
       return (T)((U)a + (U)b);  // two's-complement wraparound
     } else {
       return a + b;
+    }
+  }
+};
+template <class T> struct Op<T, OP_MUL> {
+  static __device__ __forceinline__ T f(T a, T b) {
+    if constexpr (std::is_integral<T>::value) {
+      using U = typename std::make_unsigned<T>::type;
+      return (T)((U)a * (U)b);  // the low bits of the product (two's complement)
+    } else {
+      return a * b;
     }
   }
 };

@@ -266,6 +266,7 @@ template <class T> cudaError_t launch_rts(const RtsJob& job, const LaunchCtx& ct
   switch (job.op) {
     case OP_ADD: return launch_rts_op<T, OP_ADD>(job, ctx);
     case OP_MAX: return launch_rts_op<T, OP_MAX>(job, ctx);
+    case OP_MUL: return launch_rts_op<T, OP_MUL>(job, ctx);
     default: return launch_rts_op<T, OP_MIN>(job, ctx);
   }
 }

@@ -37,6 +37,7 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
       switch (job.op) {
         case OP_ADD: return launch_seg_chunk_op<T, OP_ADD>(job, ctx);
         case OP_MAX: return launch_seg_chunk_op<T, OP_MAX>(job, ctx);
+        case OP_MUL: return launch_seg_chunk_op<T, OP_MUL>(job, ctx);
         default: return launch_seg_chunk_op<T, OP_MIN>(job, ctx);
       }
     }
@@ -45,6 +46,7 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
     switch (job.op) {
       case OP_ADD: return launch_seg_op<T, OP_ADD>(job, ctx);
       case OP_MAX: return launch_seg_op<T, OP_MAX>(job, ctx);
+      case OP_MUL: return launch_seg_op<T, OP_MUL>(job, ctx);
       default: return launch_seg_op<T, OP_MIN>(job, ctx);
     }
   }
@@ -52,6 +54,7 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
     switch (job.op) {
       case OP_ADD: return launch_stash_op<T, OP_ADD>(job, ctx);
       case OP_MAX: return launch_stash_op<T, OP_MAX>(job, ctx);
+      case OP_MUL: return launch_stash_op<T, OP_MUL>(job, ctx);
       default: return launch_stash_op<T, OP_MIN>(job, ctx);
     }
   }
@@ -59,6 +62,7 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
     switch (job.op) {
       case OP_ADD: return launch_rows_op<T, OP_ADD>(job, ctx);
       case OP_MAX: return launch_rows_op<T, OP_MAX>(job, ctx);
+      case OP_MUL: return launch_rows_op<T, OP_MUL>(job, ctx);
       default: return launch_rows_op<T, OP_MIN>(job, ctx);
     }
   }
@@ -67,6 +71,7 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
       switch (job.op) {
         case OP_ADD: return launch_lanes_rts_op<T, OP_ADD>(job, ctx);
         case OP_MAX: return launch_lanes_rts_op<T, OP_MAX>(job, ctx);
+        case OP_MUL: return launch_lanes_rts_op<T, OP_MUL>(job, ctx);
         default: return launch_lanes_rts_op<T, OP_MIN>(job, ctx);
       }
     }
@@ -74,6 +79,7 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
   switch (job.op) {
     case OP_ADD: return launch_lanes_op<T, OP_ADD>(job, ctx);
     case OP_MAX: return launch_lanes_op<T, OP_MAX>(job, ctx);
+    case OP_MUL: return launch_lanes_op<T, OP_MUL>(job, ctx);
     default: return launch_lanes_op<T, OP_MIN>(job, ctx);
   }
 }

@@ -231,20 +231,25 @@ __device__ __forceinline__ T seg_reduce_part(const T* in, long long n, long long
 }
 
 // Phase 2, by one whole warp: the combination of the aggregates of segments
-// first .. first+cnt-1 (cnt >= 1, the earlier segments of the row), waiting (bounded
-// by wait_ns) for each to be published.  Lane l owns segments first+l, first+l+32,
-// ...: all are requested at once, and only those not yet published are read again.
-// Returns the base sum in every lane.
+// first .. first+cnt-1 (1 <= cnt <= 32 M, the earlier segments of the row), waiting
+// (bounded by wait_ns) for each to be published.  Lane l owns the consecutive
+// segments first + l P .. first + l P + P - 1, P = ceil(cnt / 32): all are requested
+// at once, and only those not yet published are read again.  Every partial result
+// then combines consecutive segments in order (as the look-back's ordered combine
+// does), which keeps float products from overflowing where the prefix itself does
+// not.  Returns the base sum in every lane.
 template <class T, int OP, int M, class S>
 __device__ __forceinline__ T seg_gather(const S& st, unsigned first, unsigned cnt, unsigned long long wait_ns,
                                         bool& timed_out) {
   const int lane = threadIdx.x & 31;
   const unsigned seg = cnt;
+  const unsigned per = (cnt + 31) / 32;      // segments per lane, <= M
+  const unsigned mine = (unsigned)lane * per; // this lane's first segment (relative)
   T val[M];
   unsigned pending = 0;
 #pragma unroll
   for (int k = 0; k < M; ++k)
-    if ((unsigned)(lane + 32 * k) < seg) pending |= 1u << k;
+    if ((unsigned)k < per && mine + k < seg) pending |= 1u << k;
   unsigned long long t0 = 0;
   timed_out = false;
   for (int spins = 0;; ++spins) {
@@ -252,9 +257,9 @@ __device__ __forceinline__ T seg_gather(const S& st, unsigned first, unsigned cn
     for (int k = 0; k < M; ++k) {
       if (pending & (1u << k)) {
         T v;
-        const unsigned f = st.poll(first + lane + 32 * k, v);
+        const unsigned f = st.poll(first + mine + k, v);
         if (f != FLAG_X) {
-          val[k] = st.fetch(first + lane + 32 * k, f, v);
+          val[k] = st.fetch(first + mine + k, f, v);
           pending &= ~(1u << k);
         }
       }
@@ -274,14 +279,14 @@ __device__ __forceinline__ T seg_gather(const S& st, unsigned first, unsigned cn
     backoff(spins);
   }
   // Lane fold in segment order, then the lanes in lane order.  A lane with no
-  // segment contributes the identity of add (and of the saturating add), or (max /
-  // min being idempotent) lane 0's first value.
+  // segment contributes the neutral element of add (and of the saturating add) or
+  // of multiply, or (max / min being idempotent) lane 0's first value.
   T acc = val[0];
 #pragma unroll
   for (int k = 1; k < M; ++k)
-    if ((unsigned)(lane + 32 * k) < seg) acc = Op<T, OP>::f(acc, val[k]);
+    if ((unsigned)k < per && mine + k < seg) acc = Op<T, OP>::f(acc, val[k]);
   const T v00 = __shfl_sync(0xffffffffu, val[0], 0);
-  if ((unsigned)lane >= seg) acc = (OP == OP_ADD || OP == OP_SATADD) ? T{} : v00;
+  if (mine >= seg) acc = (OP == OP_ADD || OP == OP_SATADD) ? T{} : OP == OP_MUL ? T(1) : v00;
   const T inc = warp_inclusive<T, OP>(acc, lane);
   return __shfl_sync(0xffffffffu, inc, 31);
 }

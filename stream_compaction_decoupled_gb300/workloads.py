@@ -43,13 +43,36 @@ def small_ints(n: int, seed: int, lo: int = 0, hi: int = 100, dtype=np.int32) ->
     return rng(seed).integers(lo, hi, n, dtype=dtype)
 
 
+def lognormal(n: int, dtype, seed: int, sigma: float) -> np.ndarray:
+    """n factors exp(sigma * N(0, 1)): products of many stay within the type's range."""
+    return np.exp(sigma * rng(seed).standard_normal(n)).astype(dtype)
+
+
+def odd_ints(n: int, seed: int, dtype=np.int32) -> np.ndarray:
+    """n odd integers in [-999, 999]: their products never reach 0 modulo 2^32."""
+    return (rng(seed).integers(-999, 1000, n) | 1).astype(dtype)
+
+
+def signs_pow2(n: int, dtype, seed: int, span: int = 30) -> np.ndarray:
+    """n factors +-2^k whose running products are +-2^e with |e| <= span: every
+    partial product is exact in fp32 and fp64, in any bracketing.  The exponent
+    path is a lazy random walk folded into [-span, span] (steps of -1, 0, +1)."""
+    r = rng(seed)
+    walk = np.cumsum(r.choice(np.array([-1, 0, 1]), n, p=[0.1, 0.8, 0.1]))
+    e = span - np.abs(np.mod(walk + span, 4 * span) - 2 * span)   # folded, unit steps
+    step = np.diff(np.concatenate([[0], e]))
+    sign = r.choice(np.array([1.0, -1.0]), n, p=[0.7, 0.3])
+    return (sign * np.exp2(step)).astype(dtype)
+
+
 def poisson_counts(n: int, lam: float, seed: int) -> np.ndarray:
     """n int32 record counts k_i ~ Poisson(lam)."""
     return rng(seed).poisson(lam, n).astype(np.int32)
 
 
-def values(kind: str, n: int, dtype, seed: int) -> np.ndarray:
-    """Dispatch on a distribution name: normal, uniform01, uniform_pm1, ints, ones."""
+def values(kind: str, n: int, dtype, seed: int, extra: dict | None = None) -> np.ndarray:
+    """Dispatch on a distribution name: normal, uniform01, uniform_pm1, ints, ones,
+    lognormal (extra["sigma"]), odd_ints, signs_pow2."""
     if kind == "normal":
         return normal(n, dtype, seed)
     if kind == "uniform01":
@@ -60,6 +83,12 @@ def values(kind: str, n: int, dtype, seed: int) -> np.ndarray:
         return small_ints(n, seed, dtype=dtype)
     if kind == "ones":
         return np.ones(n, dtype=dtype)
+    if kind == "lognormal":
+        return lognormal(n, dtype, seed, (extra or {}).get("sigma", 0.005))
+    if kind == "odd_ints":
+        return odd_ints(n, seed, dtype)
+    if kind == "signs_pow2":
+        return signs_pow2(n, dtype, seed)
     raise ValueError(kind)
 
 
@@ -89,7 +118,7 @@ class Workload:
         """Generate the input (lane values flattened in row-major order)."""
         if self.kind == "pack":
             return poisson_counts(self.elems, self.extra.get("lam", 4.0), self.seed)
-        return values(self.dist, self.elems * self.lanes, self.dtype, self.seed)
+        return values(self.dist, self.elems * self.lanes, self.dtype, self.seed, self.extra)
 
 
 # The configurations, each with a fixed seed.  The headline is "fp32_1e8".
@@ -113,6 +142,15 @@ WORKLOADS = [
     Workload("struct96_3x1e5_axis1", "batched", "float32", (3, 100_000), "normal", 13, lanes=24, axis=1),
     Workload("dual16_1e6", "scan", "float64", (1_000_000,), "uniform_pm1", 14, lanes=17),
     Workload("dual16_3x1e5_axis1", "batched", "float64", (3, 100_000), "uniform_pm1", 15, lanes=17, axis=1),
+    # Beyond the kernel-time table: cumprod (the accumulate API's other reduction),
+    # the 32-byte struct the PR also measures, and its largest element (2080 bytes)
+    # with and without a neutral element.
+    Workload("fp32_1e7_cumprod", "scan", "float32", (10_000_000,), "lognormal", 16, op="mul",
+             extra={"sigma": 0.005}),
+    Workload("i32_1e6_cumprod", "scan", "int32", (1_000_000,), "odd_ints", 17, op="mul"),
+    Workload("struct32_1e6", "scan", "float32", (1_000_000,), "normal", 18, lanes=8),
+    Workload("elem2080_2e4", "scan", "float32", (20_000,), "normal", 19, lanes=520),
+    Workload("elem2080_2e4_max", "scan", "float32", (20_000,), "normal", 20, lanes=520, op="max"),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS}

@@ -4,7 +4,11 @@ Bars:
   - integers, max/min, compaction indices, packing: bit-exact (max/min on floats:
     exact value equality, since they never round);
   - float add: |gpu - oracle_fp64| <= 1e-5 * (prefix sum of |x|) + 1e-6, element
-    by element and lane by lane, the prefix sum of |x| taken along the scanned axis.
+    by element and lane by lane, the prefix sum of |x| taken along the scanned axis;
+  - float multiply: |gpu - oracle_fp64| <= gamma_k * |oracle_fp64| with k the number
+    of factors at that position (plus init) and gamma_k = k u / (1 - k u), u the unit
+    roundoff of the element type: the rounding bound of a product of k floats in any
+    bracketing (each multiplication adds a relative error of at most u).
 """
 import numpy as np
 
@@ -23,6 +27,21 @@ def assert_scan_matches(got: np.ndarray, x3: np.ndarray, op: str, inclusive: boo
     """got and x3 are (B, R, C) arrays; the oracle scans x3 along axis 1."""
     want = oracle.scan3(x3, op, inclusive, init)
     got = got.reshape(x3.shape)
+    if op == "mul" and x3.dtype.kind == "f":
+        u = 2.0 ** -24 if x3.dtype == np.float32 else 2.0 ** -53
+        k = np.arange(1, x3.shape[1] + 1, dtype=np.float64).reshape(1, -1, 1)
+        if not inclusive:
+            k = k - 1 + (0 if init is None else 1)
+        ku = k * u
+        gamma = np.where(ku < 0.5, ku / (1 - ku), np.inf)
+        err = np.abs(got.astype(np.float64) - want)
+        ok = err <= gamma * np.abs(want)
+        if not ok.all():
+            bad = np.argwhere(~ok)[:5]
+            b0 = tuple(bad[0])
+            raise AssertionError("%s: %d products out of tolerance, first at %s: got %r want %r" % (
+                what, int((~ok).sum()), list(b0), float(got[b0]), float(want[b0])))
+        return
     if x3.dtype.kind in "iu" or op != "add":
         if x3.dtype.kind == "f":
             ok = got.astype(np.float64) == want

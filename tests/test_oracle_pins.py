@@ -172,9 +172,56 @@ def pin_axes_and_lanes(scan3, golden=None):
         assert [int(v) for v in got[0, :, c]] == want
 
 
+def _wrap(v, bits, signed=True):
+    v %= 2**bits
+    return v - 2**bits if signed and v >= 2**(bits - 1) else v
+
+
+def pin_mul_closed_forms(scan3, golden=None):
+    """Multiply (cumprod): factorials, powers of two, exact sign/power-of-two
+    products, wraparound to the low bits, and the neutral element 1."""
+    x = np.arange(1, 21, dtype=np.int64)                 # 20! < 2^63
+    assert [int(v) for v in one_d(scan3, x, "mul")] == [math.factorial(k) for k in range(1, 21)]
+    xf = np.arange(1, 19, dtype=np.float64)              # 18! < 2^53: exact in fp64
+    assert [float(v) for v in one_d(scan3, xf, "mul")] == [float(math.factorial(k)) for k in range(1, 19)]
+    p = np.full(40, 2, dtype=np.int32)                   # 2^k keeps its low 32 bits
+    assert [int(v) for v in one_d(scan3, p, "mul")] == [_wrap(2**k, 32) for k in range(1, 41)]
+    e = one_d(scan3, np.array([3, 4, 5], dtype=np.int32), "mul", inclusive=False)
+    assert [int(v) for v in e] == [1, 3, 12]             # no init: starts from 1
+    e7 = one_d(scan3, np.array([3, 4, 5], dtype=np.int32), "mul", inclusive=False, init=7)
+    assert [int(v) for v in e7] == [7, 21, 84]           # init folds in on the left
+    r = np.random.default_rng(33)
+    xo = (r.integers(-999, 1000, 300) | 1).astype(np.int32)   # odd: never 0 mod 2^32
+    acc, want = 1, []
+    for v in xo:
+        acc *= int(v)
+        want.append(_wrap(acc, 32))
+    assert [int(v) for v in one_d(scan3, xo, "mul")] == want
+    xs = r.choice(np.array([1.0, -1.0, 2.0, 0.5], dtype=np.float32), 2000, p=[0.4, 0.3, 0.15, 0.15])
+    acc, wantf = 1, []
+    for v in xs:                                         # products of +-2^k are exact
+        acc = acc * float(v)
+        wantf.append(acc)
+    assert [float(v) for v in one_d(scan3, xs, "mul")] == wantf
+
+
+def pin_mul_bruteforce(scan3, golden=None):
+    r = np.random.default_rng(77)
+    for n in (1, 2, 33, 200):
+        xi = r.integers(-50, 50, n).astype(np.int64)
+        got = [int(v) for v in one_d(scan3, xi, "mul")]
+        assert got == [_wrap(math.prod(int(v) for v in xi[: i + 1]), 64) for i in range(n)]
+        xf = np.exp(r.standard_normal(n) * 0.3)
+        got = one_d(scan3, xf, "mul")
+        want = np.array([math.prod(float(v) for v in xf[: i + 1]) for i in range(n)])
+        eps = np.finfo(np.float64).eps
+        assert np.all(np.abs(got - want) <= 2 * (np.arange(n) + 1) * eps * np.abs(want))
+
+
 PINS = [pin_golden_definitions, pin_golden_kogge_stone, pin_golden_kary, pin_all_ones,
         pin_last_is_reduction, pin_max_min_monotone, pin_exclusive_relations,
-        pin_wraparound, pin_bruteforce, pin_axes_and_lanes]
+        pin_wraparound, pin_bruteforce, pin_axes_and_lanes, pin_mul_closed_forms,
+        pin_mul_bruteforce]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -217,13 +264,19 @@ def _numpy_scan3(mistake):
         use = op
         if mistake == "max_is_min":
             use = {"max": "min", "min": "max"}.get(op, op)
+        if mistake == "mul_is_add":
+            use = {"mul": "add"}.get(op, op)
         if mistake == "drop_first_term":
             a = a.copy()
             idx = [slice(None)] * 3
             idx[axis] = 0
             if use == "add":
                 a[tuple(idx)] = 0
-        if use == "add":
+            if use == "mul":
+                a[tuple(idx)] = 1
+        if use == "mul":
+            s = np.cumprod(a, axis=axis, dtype=acc_t)
+        elif use == "add":
             if mistake == "wrong_sign":
                 s = np.cumsum(-a, axis=axis) + 2 * np.take(a, [0], axis=axis)
             else:
@@ -239,9 +292,13 @@ def _numpy_scan3(mistake):
         if inclusive:
             return s
         first = np.zeros_like(np.take(s, [0], axis=axis))
+        if use == "mul" and mistake != "mul_identity_zero":
+            first = first + 1
         if init is not None and mistake != "init_ignored":
-            first = first + np.asarray(init, dtype=acc_t).reshape(1, 1, -1)
-            if use == "add":
+            first = first * 0 + np.asarray(init, dtype=acc_t).reshape(1, 1, -1)
+            if use == "mul":
+                s = s * np.asarray(init, dtype=acc_t).reshape(1, 1, -1)
+            elif use == "add":
                 s = s + np.asarray(init, dtype=acc_t).reshape(1, 1, -1)
             elif use == "max":
                 s = np.maximum(s, np.asarray(init, dtype=acc_t).reshape(1, 1, -1))
@@ -253,7 +310,7 @@ def _numpy_scan3(mistake):
 
 
 MISTAKES = ["drop_first_term", "wrong_sign", "off_by_one", "reversed", "transposed_axis",
-            "max_is_min", "init_ignored", "fp32_accumulate"]
+            "max_is_min", "init_ignored", "fp32_accumulate", "mul_is_add", "mul_identity_zero"]
 
 
 def test_reference_numpy_scan_passes(golden):
