@@ -65,6 +65,7 @@ KERNEL_SOURCES = {
     "scan_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh"),
     "compact_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "compact.cuh"),
     "compact_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "compact.cuh"),
+    "partition_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "compact.cuh", "partition.cuh"),
     "scan_lanes_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh"),
     "pack_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "pack.cu"),
     "pack_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "pack.cu"),
@@ -271,6 +272,13 @@ def workload_call(w, device):
         torch.cuda.synchronize()
         m = int(cnt.item())
         return fn, 4 * x.numel() + 4 * m + 4, x.numel(), "Gelem/s"
+    if w.kind == "partition":  # values and their input indices
+        out = torch.empty_like(x)
+        idx = torch.empty(x.numel(), dtype=torch.int32, device=device)
+        cnt = torch.empty(1, dtype=torch.int32, device=device)
+        p = w.extra["p"]
+        fn = lambda: gb.partition(x, "lt", p, out=out, out_idx=idx, out_count=cnt)  # noqa: E731
+        return fn, 2 * x.numel() * es + 4 * x.numel() + 4, x.numel(), "Gelem/s"
     total = int(x.sum().item())  # pack
     recs = torch.empty(total, dtype=torch.int32, device=device)
     tot = torch.empty(1, dtype=torch.int32, device=device)

@@ -72,8 +72,11 @@ enum gb_dtype { GB_I32 = 0, GB_U32 = 1, GB_I64 = 2, GB_U64 = 3, GB_F32 = 4, GB_F
  * unit roundoff of the type). */
 enum gb_op { GB_ADD = 0, GB_MAX = 1, GB_MIN = 2, GB_MUL = 3 };
 
-/* Compaction predicates: element x is selected when  x <op> threshold. */
-enum gb_pred { GB_LT = 0, GB_LE = 1, GB_GT = 2, GB_GE = 3, GB_EQ = 4, GB_NE = 5 };
+/* Compaction and partition predicates: element x is selected when  x <op> threshold,
+ * compared in the element type (a NaN fails every comparison but NE).  GB_BIT_CLEAR
+ * (partition, integer types): x is selected when bit `threshold` (0 .. bits - 1) of
+ * x is 0 -- the one-bit split of a radix sort. */
+enum gb_pred { GB_LT = 0, GB_LE = 1, GB_GT = 2, GB_GE = 3, GB_EQ = 4, GB_NE = 5, GB_BIT_CLEAR = 6 };
 
 /* Kinds for gb_temp_storage_bytes. */
 enum gb_kind {
@@ -82,7 +85,8 @@ enum gb_kind {
   GB_KIND_BATCHED_AXIS0 = 2, /* gb_scan_batched axis 0: rows x cols                   */
   GB_KIND_COMPACT = 3,       /* gb_compact: rows = n                                  */
   GB_KIND_PACK = 4,          /* gb_pack_by_counts: rows = n                           */
-  GB_KIND_REDUCE_THEN_SCAN = 5 /* gb_scan_reduce_then_scan: rows = n                  */
+  GB_KIND_REDUCE_THEN_SCAN = 5, /* gb_scan_reduce_then_scan: rows = n                 */
+  GB_KIND_PARTITION = 6        /* gb_partition: rows = n                              */
 };
 
 /* Status codes. */
@@ -145,6 +149,25 @@ int gb_scan_batched(int dtype, int lanes, int op, int inclusive, const void* in,
 int gb_compact(int dtype, const void* in, int64_t n, int pred, const void* threshold,
                int32_t* out_idx, int32_t* out_count, void* temp, size_t temp_bytes,
                void* stream);
+
+/*
+ * Stable partition ([PS] "Other Applications": partitioning, and the split that a
+ * radix sort repeats; "Solution": count, scan, emit, here with two destinations):
+ * the elements x_i (lanes = 1) with  x_i <pred> *threshold  go first, in input
+ * order, then all the others, in input order.
+ *   out        n elements of `dtype` (device): out[0 .. m) selected, out[m .. n) the rest
+ *   out_idx    n int32 (device) or NULL: the input index of each element of out
+ *   out_count  one int32 (device): m
+ * pred is a gb_pred; GB_BIT_CLEAR (integer dtypes only) selects the elements whose
+ * bit *threshold is 0.  `in` must hold naturally aligned elements and must not
+ * overlap out or out_idx.  One launch with every CTA resident at once (cooperative):
+ * count, gather all segments' counts, rescan and write both windows.
+ * Errors: GB_ERR_RANGE if n > INT32_MAX; GB_ERR_UNSUPPORTED for GB_BIT_CLEAR on
+ * floats; GB_ERR_INVALID for a bit index outside the type.  temp kind:
+ * GB_KIND_PARTITION.
+ */
+int gb_partition(int dtype, const void* in, int64_t n, int pred, const void* threshold, void* out,
+                 int32_t* out_idx, int32_t* out_count, void* temp, size_t temp_bytes, void* stream);
 
 /*
  * Variable-length packing ([PS] "Output Format" and "Solution"): object i emits

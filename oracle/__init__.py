@@ -8,7 +8,7 @@ The arithmetic lives in ``oracle.c`` (plain C, one left-to-right loop per scanne
 line, fp64 accumulation for floating point); this module only builds it, loads it
 with ctypes and marshals numpy arrays.  Definitions followed are those of
 B. Merry, "Prefix sums on GPUs" (slides "Exclusive Prefix Sum", "Inclusive Prefix
-Sum", "Output Format", "Solution", "Other Applications").
+Sum", "Output Format", "Solution", "Other Applications": compaction, partitioning).
 """
 from __future__ import annotations
 
@@ -27,7 +27,7 @@ _DTYPES = {"i32": 0, "u32": 1, "i64": 2, "u64": 3, "f32": 4, "f64": 5}
 _NP = {"i32": np.int32, "u32": np.uint32, "i64": np.int64, "u64": np.uint64,
        "f32": np.float32, "f64": np.float64}
 _OPS = {"add": 0, "max": 1, "min": 2, "mul": 3}
-_PREDS = {"lt": 0, "le": 1, "gt": 2, "ge": 3, "eq": 4, "ne": 5}
+_PREDS = {"lt": 0, "le": 1, "gt": 2, "ge": 3, "eq": 4, "ne": 5, "bit_clear": 6}
 
 _lib = None
 
@@ -51,6 +51,8 @@ def _load():
         lib.oracle_scan.restype = i
         lib.oracle_compact.argtypes = [i, vp, i64, i, vp, vp]
         lib.oracle_compact.restype = i64
+        lib.oracle_partition.argtypes = [i, vp, i64, i, vp, vp, vp]
+        lib.oracle_partition.restype = i64
         lib.oracle_pack_by_counts.argtypes = [vp, i64, vp, vp, i64]
         lib.oracle_pack_by_counts.restype = i64
         _lib = lib
@@ -130,6 +132,22 @@ def compact(x: np.ndarray, pred: str, threshold) -> np.ndarray:
     if cnt < 0:
         raise ValueError("oracle_compact rejected its arguments (%d)" % cnt)
     return out[:cnt].copy()
+
+
+def partition(x: np.ndarray, pred: str, threshold):
+    """Stable partition: (values, int64 input indices, m).  The m elements with
+    pred(x[i], threshold) come first, then the others, each in input order;
+    pred "bit_clear" (integers) selects the elements whose bit `threshold` is 0."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    dt = dtype_name(x)
+    t = np.asarray(threshold, dtype=x.dtype).reshape(1)
+    vals = np.empty(max(x.size, 1), dtype=x.dtype)
+    idx = np.empty(max(x.size, 1), dtype=np.int64)
+    m = _load().oracle_partition(_DTYPES[dt], x.ctypes.data, x.size, _PREDS[pred], t.ctypes.data,
+                                 vals.ctypes.data, idx.ctypes.data)
+    if m < 0:
+        raise ValueError("oracle_partition rejected its arguments (%d)" % m)
+    return vals[:x.size].copy(), idx[:x.size].copy(), int(m)
 
 
 def pack_by_counts(counts: np.ndarray, capacity: int | None = None):

@@ -43,13 +43,14 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <string.h>
 
 /* Element types, operators and predicates, numbered for the Python wrapper
  * in oracle/__init__.py (its own table; nothing here is shared with the GPU
  * library). */
 enum { OR_I32 = 0, OR_U32 = 1, OR_I64 = 2, OR_U64 = 3, OR_F32 = 4, OR_F64 = 5 };
 enum { OR_ADD = 0, OR_MAX = 1, OR_MIN = 2, OR_MUL = 3 };
-enum { OR_LT = 0, OR_LE = 1, OR_GT = 2, OR_GE = 3, OR_EQ = 4, OR_NE = 5 };
+enum { OR_LT = 0, OR_LE = 1, OR_GT = 2, OR_GE = 3, OR_EQ = 4, OR_NE = 5, OR_BITCLR = 6 };
 
 #define OR_OK 0
 #define OR_BAD_ARGUMENT (-1)
@@ -290,6 +291,56 @@ int64_t oracle_compact(int dtype, const void *in, int64_t n, int pred,
     for (int64_t i = 0; i < n; i++)
         if (selected(dtype, pred, in, i, threshold)) out_idx[count++] = i;
     return count;
+}
+
+/* ---- partition ----------------------------------------------------------- */
+
+/* Is bit b of the element's bit pattern clear?  (Integer types.) */
+static int bit_clear(int dtype, const void *in, int64_t i, uint64_t b)
+{
+    uint64_t v;
+    switch (dtype) {
+    case OR_I32: v = (uint32_t)((const int32_t *)in)[i]; break;
+    case OR_U32: v = ((const uint32_t *)in)[i]; break;
+    case OR_I64: v = (uint64_t)((const int64_t *)in)[i]; break;
+    default: v = ((const uint64_t *)in)[i]; break;
+    }
+    return ((v >> b) & 1u) == 0;
+}
+
+/*
+ * Stable partition (slides "Other Applications": partitioning, and the split
+ * step of radix sort): out receives first every element that satisfies the
+ * predicate, in input order, then every other element, in input order;
+ * out_idx[k] is the input index of out[k].  Predicates as for compaction, plus
+ * OR_BITCLR for integer types: bit *threshold (as an unsigned bit index) of x
+ * is 0.  out holds n elements of the input type, out_idx n entries.  Returns
+ * the number selected, or a negative error code.
+ */
+int64_t oracle_partition(int dtype, const void *in, int64_t n, int pred,
+                         const void *threshold, void *out, int64_t *out_idx)
+{
+    if (n < 0 || dtype < OR_I32 || dtype > OR_F64) return OR_BAD_ARGUMENT;
+    if (pred < OR_LT || pred > OR_BITCLR) return OR_BAD_ARGUMENT;
+    size_t es = (dtype == OR_I32 || dtype == OR_U32 || dtype == OR_F32) ? 4 : 8;
+    uint64_t bit = 0;
+    if (pred == OR_BITCLR) {
+        if (dtype == OR_F32 || dtype == OR_F64) return OR_BAD_ARGUMENT;
+        if (es == 4) bit = *(const uint32_t *)threshold;
+        else bit = *(const uint64_t *)threshold;
+        if (bit >= 8 * es) return OR_BAD_ARGUMENT;
+    }
+    int64_t k = 0, m = 0;
+    for (int pass = 1; pass >= 0; pass--)   /* the selected ones, then the rest */
+        for (int64_t i = 0; i < n; i++) {
+            int s = pred == OR_BITCLR ? bit_clear(dtype, in, i, bit)
+                                      : selected(dtype, pred, in, i, threshold);
+            if (s != pass) continue;
+            memcpy((char *)out + k * es, (const char *)in + i * es, es);
+            out_idx[k++] = i;
+            if (pass) m++;
+        }
+    return m;
 }
 
 /* ---- packing by counts --------------------------------------------------- */

@@ -20,12 +20,13 @@ LIB_PATH = os.path.join(_HERE, "libgbscan.so")
 # Mirrors of the enums in include/gbscan.h.
 I32, U32, I64, U64, F32, F64 = range(6)
 ADD, MAX, MIN, MUL = range(4)
-LT, LE, GT, GE, EQ, NE = range(6)
-KIND_SCAN, KIND_BATCHED_AXIS1, KIND_BATCHED_AXIS0, KIND_COMPACT, KIND_PACK, KIND_REDUCE_THEN_SCAN = range(6)
+LT, LE, GT, GE, EQ, NE, BIT_CLEAR = range(7)
+KIND_SCAN, KIND_BATCHED_AXIS1, KIND_BATCHED_AXIS0, KIND_COMPACT, KIND_PACK, KIND_REDUCE_THEN_SCAN, \
+    KIND_PARTITION = range(7)
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_TEMP, ERR_NO_IDENTITY, ERR_RANGE, ERR_CUDA, ERR_TIMEOUT = range(8)
 
 OPS = {"add": ADD, "max": MAX, "min": MIN, "mul": MUL}
-PREDS = {"lt": LT, "le": LE, "gt": GT, "ge": GE, "eq": EQ, "ne": NE}
+PREDS = {"lt": LT, "le": LE, "gt": GT, "ge": GE, "eq": EQ, "ne": NE, "bit_clear": BIT_CLEAR}
 _NP_OF = {I32: np.int32, U32: np.uint32, I64: np.int64, U64: np.uint64, F32: np.float32, F64: np.float64}
 
 # Exported symbols and their ctypes signatures (the whole of include/gbscan.h).
@@ -35,6 +36,7 @@ SIGNATURES = {
     "gb_scan_exclusive": (_i, [_i, _i, _i, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "gb_scan_batched": (_i, [_i, _i, _i, _i, _vp, _vp, _i64, _i64, _i, _vp, _vp, _sz, _vp]),
     "gb_compact": (_i, [_i, _vp, _i64, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "gb_partition": (_i, [_i, _vp, _i64, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "gb_pack_by_counts": (_i, [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "gb_scan_reduce_then_scan": (_i, [_i, _i, _i, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "gb_temp_storage_bytes": (_sz, [_i, _i, _i, _i64, _i64]),
@@ -190,6 +192,29 @@ def compact(x, pred: str, threshold, out_idx=None, out_count=None, temp=None, st
                              tp, tb, _stream(x, stream)), "gb_compact")
     del keep
     return out_idx, out_count
+
+
+def partition(x, pred: str, threshold, with_idx: bool = True, out=None, out_idx=None, out_count=None, temp=None,
+              stream=None):
+    """Stable partition: (out, out_idx or None, count (device int32)); out holds the
+    elements with x <pred> threshold first, then the others, each in input order.
+    pred "bit_clear" (integers) selects the elements whose bit `threshold` is 0."""
+    import torch
+    n = x.numel()
+    out = torch.empty(max(n, 1), dtype=x.dtype, device=x.device) if out is None else out
+    if with_idx and out_idx is None:
+        out_idx = torch.empty(max(n, 1), dtype=torch.int32, device=x.device)
+    out_count = torch.empty(1, dtype=torch.int32, device=x.device) if out_count is None else out_count
+    _need_cuda(x, out, out_count)
+    code = dtype_code(x.dtype)
+    keep, tptr = _host_value(code, threshold, 1)
+    tp, tb = _temp(x, KIND_PARTITION, code, 1, n, 0, temp)
+    _check(load().gb_partition(code, ctypes.c_void_p(x.data_ptr()), n, PREDS[pred], tptr,
+                               ctypes.c_void_p(out.data_ptr()),
+                               ctypes.c_void_p(out_idx.data_ptr()) if out_idx is not None else None,
+                               ctypes.c_void_p(out_count.data_ptr()), tp, tb, _stream(x, stream)), "gb_partition")
+    del keep
+    return out, out_idx, out_count
 
 
 def pack_by_counts(counts, capacity: int, offsets: bool = True, out_records=None, out_total=None,

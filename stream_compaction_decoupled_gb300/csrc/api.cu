@@ -414,6 +414,51 @@ int gb_compact(int dtype, const void* in, int64_t n, int pred, const void* thres
   return e == cudaSuccess ? GB_OK : cuda_fail(e);
 }
 
+int gb_partition(int dtype, const void* in, int64_t n, int pred, const void* threshold, void* out,
+                 int32_t* out_idx, int32_t* out_count, void* temp, size_t temp_bytes, void* stream) {
+  if (!dtype_size(dtype) || pred < GB_LT || pred > GB_BIT_CLEAR || n < 0) return GB_ERR_INVALID;
+  if (!out_count || !threshold) return GB_ERR_INVALID;
+  const bool is_float = dtype == GB_F32 || dtype == GB_F64;
+  if (pred == GB_BIT_CLEAR) {
+    if (is_float) return GB_ERR_UNSUPPORTED;
+    unsigned long long b = 0;
+    std::memcpy(&b, threshold, dtype_size(dtype));
+    if (dtype == GB_I32 || dtype == GB_U32) b &= 0xffffffffull;
+    if (b >= 8 * dtype_size(dtype)) return GB_ERR_INVALID;
+  }
+  if (n > 0x7fffffffll) return GB_ERR_RANGE;
+  if (n > 0 && (!in || !out)) return GB_ERR_INVALID;
+  if (n > 0 && (uintptr_t)in % dtype_size(dtype) != 0) return GB_ERR_INVALID;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  if (n == 0) {
+    cudaError_t e = cudaMemsetAsync(out_count, 0, sizeof(int32_t), ctx.stream);
+    return e == cudaSuccess ? GB_OK : cuda_fail(e);
+  }
+  const size_t need = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::partition_temp_bytes<T>();
+  });
+  Temp t;
+  rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
+  if (rc) return rc;
+  gbs::PartitionJob job;
+  job.in = in;
+  job.n = n;
+  job.pred = pred;
+  job.threshold_host = threshold;
+  job.out = out;
+  job.out_idx = out_idx;
+  job.out_count = out_count;
+  job.temp = t.p;
+  const cudaError_t e = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::launch_partition<T>(job, ctx);
+  });
+  return e == cudaSuccess ? GB_OK : cuda_fail(e);
+}
+
 int gb_pack_by_counts(const int32_t* counts, int64_t n, int32_t* offsets, int32_t* out_records,
                       int64_t out_capacity, int32_t* out_total, void* temp, size_t temp_bytes, void* stream) {
   if (n < 0 || out_capacity < 0 || !out_total) return GB_ERR_INVALID;
@@ -490,6 +535,11 @@ size_t gb_temp_storage_bytes(int kind, int dtype, int lanes, int64_t rows, int64
       });
     case GB_KIND_PACK:
       return gbs::pack_temp_bytes(rows);
+    case GB_KIND_PARTITION:
+      return with_type(dtype, [&](auto* tp) {
+        using T = std::remove_pointer_t<decltype(tp)>;
+        return gbs::partition_temp_bytes<T>();
+      });
     case GB_KIND_REDUCE_THEN_SCAN:
       return with_type(dtype, [&](auto* tp) {
         using T = std::remove_pointer_t<decltype(tp)>;

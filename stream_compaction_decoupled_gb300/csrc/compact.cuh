@@ -50,7 +50,11 @@ template <int PRED, class T> __device__ __forceinline__ bool select_pred(T x, T 
   else if constexpr (PRED == 2) return x > t;
   else if constexpr (PRED == 3) return x >= t;
   else if constexpr (PRED == 4) return x == t;
-  else return !(x == t);
+  else if constexpr (PRED == 5) return !(x == t);
+  else {  // 6, integers only: bit t of x is clear (the one-bit split)
+    using U = typename std::make_unsigned<T>::type;
+    return (((U)x >> (unsigned)t) & 1u) == 0;
+  }
 }
 
 template <class T>

@@ -1,6 +1,7 @@
 // inst_f64.cu -- every kernel launcher for double elements (one translation unit per
 // element type, so the library builds in parallel).
 #include "compact.cuh"
+#include "partition.cuh"
 #include "rts.cuh"
 #include "scan.cuh"
 

@@ -48,6 +48,17 @@ struct CompactJob {
   void* temp = nullptr;
 };
 
+struct PartitionJob {
+  const void* in = nullptr;
+  long long n = 0;
+  int pred = 0;  // gb_pred, or 6 (bit clear, integers)
+  const void* threshold_host = nullptr;
+  void* out = nullptr;
+  int32_t* out_idx = nullptr;
+  int32_t* out_count = nullptr;
+  void* temp = nullptr;
+};
+
 struct PackJob {
   const int32_t* counts = nullptr;
   long long n = 0;
@@ -74,6 +85,8 @@ template <class T> size_t scan_temp_bytes(long long B, long long R, long long C)
 template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& ctx);
 template <class T> size_t compact_temp_bytes(long long n);
 template <class T> cudaError_t launch_compact(const CompactJob& job, const LaunchCtx& ctx);
+template <class T> size_t partition_temp_bytes();
+template <class T> cudaError_t launch_partition(const PartitionJob& job, const LaunchCtx& ctx);
 template <class T> size_t rts_temp_bytes(long long n, int num_sms);
 template <class T> cudaError_t launch_rts(const RtsJob& job, const LaunchCtx& ctx);
 size_t pack_temp_bytes(long long n);

@@ -96,7 +96,7 @@ def values(kind: str, n: int, dtype, seed: int, extra: dict | None = None) -> np
 class Workload:
     """One benchmark configuration: what to scan or compact, and its seed."""
     name: str
-    kind: str            # "scan", "batched", "compact", "pack"
+    kind: str            # "scan", "batched", "compact", "pack", "partition"
     dtype: str           # numpy dtype name of one lane
     shape: tuple         # (n,) or (rows, cols)
     dist: str
@@ -151,6 +151,8 @@ WORKLOADS = [
     Workload("struct32_1e6", "scan", "float32", (1_000_000,), "normal", 18, lanes=8),
     Workload("elem2080_2e4", "scan", "float32", (20_000,), "normal", 19, lanes=520),
     Workload("elem2080_2e4_max", "scan", "float32", (20_000,), "normal", 20, lanes=520, op="max"),
+    # Stable partition (x < 0.5 first) of the compaction input's shape, values and indices.
+    Workload("partition_p0.5", "partition", "float32", (10_000_000,), "uniform01", 21, extra={"p": 0.5}),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS}

@@ -58,7 +58,7 @@ def stall():
 
 
 @pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "lanes_wide", "segments", "segments_f64",
-                                  "compact_segments", "compact_tiles", "pack", "l2_resident"])
+                                  "compact_segments", "compact_tiles", "pack", "l2_resident", "partition"])
 def test_stalled_tile_times_out(stall, kind):
     n = 64 * 4096 if kind != "l2_resident" else 26_000_000
     x = workloads.uniform01(n, np.float32, 1)
@@ -80,6 +80,8 @@ def test_stalled_tile_times_out(stall, kind):
         gb.scan_inclusive(dev(x))
     elif kind == "compact_segments":
         gb.compact(dev(x), "lt", 0.5)
+    elif kind == "partition":  # every segment waits for all counts; segment 3 never publishes
+        gb.partition(dev(x), "lt", 0.5)
     elif kind == "compact_tiles":
         gb.compact(dev(np.concatenate([x[:1], x]))[1:], "lt", 0.5)
     else:

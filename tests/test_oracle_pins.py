@@ -381,3 +381,58 @@ def test_pack_invariants():
     # empty input and all-zero counts
     assert oracle.pack_by_counts(np.zeros(0, np.int32))[2] == 0
     assert oracle.pack_by_counts(np.zeros(10, np.int32))[2] == 0
+
+
+# -------------------------------------------------------------- partition --
+
+_PYPRED = {"lt": lambda v, t: v < t, "le": lambda v, t: v <= t, "gt": lambda v, t: v > t,
+           "ge": lambda v, t: v >= t, "eq": lambda v, t: v == t, "ne": lambda v, t: not (v == t)}
+
+
+def test_partition_against_the_definition():
+    """Selected elements in input order, then the rest in input order (list comprehensions)."""
+    r = np.random.default_rng(61)
+    for dt in (np.int32, np.uint32, np.int64, np.uint64, np.float32, np.float64):
+        x = r.integers(0, 100, 3001).astype(dt)
+        for pred, f in _PYPRED.items():
+            vals, idx, m = oracle.partition(x, pred, 37)
+            sel = [i for i in range(x.size) if f(x[i], dt(37))]
+            rest = [i for i in range(x.size) if not f(x[i], dt(37))]
+            assert [int(i) for i in idx] == sel + rest and m == len(sel)
+            assert np.array_equal(vals, x[idx])
+
+
+def test_partition_bit_split_and_radix_sort():
+    """The one-bit split equals numpy's stable argsort of that bit, and 32 splits from
+    the lowest bit up (an LSD radix sort) sort unsigned keys like numpy.sort."""
+    r = np.random.default_rng(62)
+    x = r.integers(-2**31, 2**31, 5000).astype(np.int32)
+    for b in (0, 7, 31):
+        vals, idx, m = oracle.partition(x, "bit_clear", b)
+        key = (x.view(np.uint32) >> np.uint32(b)) & np.uint32(1)
+        assert np.array_equal(idx, np.argsort(key, kind="stable"))
+        assert m == int((key == 0).sum()) and np.array_equal(vals, x[idx])
+    xu = r.integers(0, 2**32, 3000, dtype=np.uint64).astype(np.uint32)
+    y = xu.copy()
+    for b in range(32):
+        y, _, _ = oracle.partition(y, "bit_clear", b)
+    assert np.array_equal(y, np.sort(xu))
+    x64 = r.integers(-2**62, 2**62, 2000).astype(np.int64)
+    _, idx, _ = oracle.partition(x64, "bit_clear", 40)
+    assert np.array_equal(idx, np.argsort((x64.view(np.uint64) >> np.uint64(40)) & np.uint64(1), kind="stable"))
+
+
+def test_partition_special_cases():
+    x = np.array([3.0, np.nan, -1.0, np.nan, 2.0], dtype=np.float32)
+    vals, idx, m = oracle.partition(x, "lt", 2.5)      # NaN fails <: it goes with the rest
+    assert list(idx) == [2, 4, 0, 1, 3] and m == 2
+    _, idx, m = oracle.partition(x, "ne", 3.0)          # ... and passes !=
+    assert list(idx) == [1, 2, 3, 4, 0] and m == 4
+    y = np.arange(10, dtype=np.int32)
+    assert oracle.partition(y, "lt", 0)[2] == 0 and list(oracle.partition(y, "lt", 0)[1]) == list(range(10))
+    assert oracle.partition(y, "ge", 0)[2] == 10
+    assert oracle.partition(np.zeros(0, np.int32), "lt", 1)[2] == 0
+    with pytest.raises(ValueError):
+        oracle.partition(y, "bit_clear", 32)             # no bit 32 in int32
+    with pytest.raises(ValueError):
+        oracle.partition(x, "bit_clear", 1)              # floats have no bit split
