@@ -6,7 +6,8 @@
 //      earlier ones give the segment's selected base, all of them the total m;
 //   3. each warp rescans its part from L2 and writes a round's selected elements to
 //      out[base + rank] and its rejected ones to out[m + (elements before - selected
-//      before) + rank], both in input order.
+//      before) + rank], both in input order (staged back to back in shared memory and
+//      stored in one pass).
 // Phase 2 waits for later segments too, so every segment must be resident at once:
 // the kernel is launched cooperatively (one CTA per SM at most).  Inputs larger than
 // L2 run the same way; their phase 3 then reads HBM again.
@@ -36,7 +37,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) partition_seg_kernel(Partition
   __shared__ unsigned s_seg;
   __shared__ unsigned s_warp[NW];
   __shared__ unsigned s_base, s_total;
-  __shared__ T s_val_all[NW * SLOTS];  // a round's selected values from the front, rejected from the back
+  __shared__ T s_val_all[NW * SLOTS];  // a round's selected values, then its rejected ones
   __shared__ int s_idx_all[NW * SLOTS];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   T* s_val = s_val_all + warp * SLOTS;
@@ -57,7 +58,27 @@ __global__ void __launch_bounds__(G::NT, G::MINB) partition_seg_kernel(Partition
     const long long v1 = e1 / VEC;
     const uint4* p = reinterpret_cast<const uint4*>(a.in);
     long long v = c0 * CH / VEC + lane;
-    for (; v < v1; v += 32 * U) {
+    if (v < 32 && v < v1) {  // the first vector of the base may hold masked elements
+      Vec<T> x;
+      const uint4 u = ld_hint(p + v, keep);
+      memcpy(x.v, &u, 16);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) cnt += (v * VEC + e >= d && select_pred<PRED>(x.v[e], a.thr)) ? 1u : 0u;
+      v += 32;
+    }
+    for (; v + 32 * (U - 1) < v1; v += 32 * U) {  // U loads in flight
+      uint4 u[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        Vec<T> x;
+        memcpy(x.v, &u[k], 16);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], a.thr) ? 1u : 0u;
+      }
+    }
+    if (v < v1) {  // the rest in one guarded round
       uint4 u[U];
 #pragma unroll
       for (int k = 0; k < U; ++k)
@@ -67,9 +88,8 @@ __global__ void __launch_bounds__(G::NT, G::MINB) partition_seg_kernel(Partition
         if (v + 32 * k < v1) {
           Vec<T> x;
           memcpy(x.v, &u[k], 16);
-          const long long pos0 = (v + 32 * k) * VEC;
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) cnt += (pos0 + e >= d && select_pred<PRED>(x.v[e], a.thr)) ? 1u : 0u;
+          for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], a.thr) ? 1u : 0u;
         }
     }
     if (lane == 0)
@@ -116,42 +136,58 @@ __global__ void __launch_bounds__(G::NT, G::MINB) partition_seg_kernel(Partition
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) {
       const unsigned p0 = cbase + (unsigned)((j * 32 + lane) * VEC);
-      unsigned sbits = 0, rbits = 0, sb = 0, st_ = 0, rb = 0, rt = 0;
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const bool valid = full || (p0 + e >= d32 && p0 + e < nb);
-        const bool s = valid && select_pred<PRED>(x[j].v[e], a.thr);
-        const bool r = valid && !s;
-        const unsigned bs = __ballot_sync(0xffffffffu, s), br = __ballot_sync(0xffffffffu, r);
-        sb += __popc(bs & lt);
-        st_ += __popc(bs);
-        rb += __popc(br & lt);
-        rt += __popc(br);
-        sbits |= (unsigned)s << e;
-        rbits |= (unsigned)r << e;
-      }
-      if (st_ + rt != 0) {  // warp-uniform
-        __syncwarp();
-        unsigned rs = sb, rr = rb;
+      // Ranks: selected elements of the lanes before this one (sb), the round's
+      // selected (st_) and rejected (rt) totals; in a full chunk every element is
+      // valid, so the rejected ones follow from the selected ones.
+      unsigned sbits = 0, rbits = 0, sb = 0, st_ = 0, rb, rt;
+      if (full) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-          const int idx = (int)(p0 + e - d32);
-          if ((sbits >> e) & 1u) {
-            s_val[rs] = x[j].v[e];
-            s_idx[rs] = idx;
-            ++rs;
-          } else if ((rbits >> e) & 1u) {
-            s_val[SLOTS - 1 - rr] = x[j].v[e];
-            s_idx[SLOTS - 1 - rr] = idx;
-            ++rr;
+          const bool s = select_pred<PRED>(x[j].v[e], a.thr);
+          const unsigned bs = __ballot_sync(0xffffffffu, s);
+          sb += __popc(bs & lt);
+          st_ += __popc(bs);
+          sbits |= (unsigned)s << e;
+        }
+        rbits = ~sbits & ((1u << VEC) - 1u);
+        rb = (unsigned)lane * VEC - sb;
+        rt = SLOTS - st_;
+      } else {
+        rb = rt = 0;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const bool valid = p0 + e >= d32 && p0 + e < nb;
+          const bool s = valid && select_pred<PRED>(x[j].v[e], a.thr);
+          const bool r = valid && !s;
+          const unsigned bs = __ballot_sync(0xffffffffu, s), br = __ballot_sync(0xffffffffu, r);
+          sb += __popc(bs & lt);
+          st_ += __popc(bs);
+          rb += __popc(br & lt);
+          rt += __popc(br);
+          sbits |= (unsigned)s << e;
+          rbits |= (unsigned)r << e;
+        }
+      }
+      if (st_ + rt != 0) {  // warp-uniform
+        // Stage the selected elements at [0, st_) and the rejected at [st_, st_ + rt),
+        // each in input order, then write both windows in one pass.
+        __syncwarp();
+        unsigned rs = sb, rr = st_ + rb;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const bool sel_e = (sbits >> e) & 1u, rej_e = (rbits >> e) & 1u;
+          if (sel_e || rej_e) {
+            const unsigned slot = sel_e ? rs++ : rr++;
+            s_val[slot] = x[j].v[e];
+            s_idx[slot] = (int)(p0 + e - d32);
           }
         }
         __syncwarp();
-        for (unsigned k = lane; k < st_; k += 32) a.out[sel + k] = s_val[k];
-        for (unsigned k = lane; k < rt; k += 32) a.out[total + rej + k] = s_val[SLOTS - 1 - k];
-        if (a.out_idx) {
-          for (unsigned k = lane; k < st_; k += 32) a.out_idx[sel + k] = s_idx[k];
-          for (unsigned k = lane; k < rt; k += 32) a.out_idx[total + rej + k] = s_idx[SLOTS - 1 - k];
+        const unsigned all = st_ + rt, rdst = total + rej - st_;
+        for (unsigned k = lane; k < all; k += 32) {
+          const unsigned dst = k < st_ ? sel + k : rdst + k;
+          a.out[dst] = s_val[k];
+          if (a.out_idx) a.out_idx[dst] = s_idx[k];
         }
         sel += st_;
         rej += rt;
