@@ -70,6 +70,7 @@ KERNEL_SOURCES = {
     "pack_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "pack.cu"),
     "pack_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "pack.cu"),
     "rts_scan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "rts.cuh"),
+    "stf_fan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "rts.cuh"),
     "lanes_rts_reduce_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
     "lanes_rts_spine_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
     "lanes_rts_scan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
@@ -327,20 +328,27 @@ def secondary_workloads(device, hbm_peak, reps=10, only=None):
                        "throughput": round(units / (ms * 1e-3) / 1e9, 3), "throughput_unit": unit,
                        "algorithmic_bytes": int(nbytes), "l2": "flushed between repetitions"}
         del fn
-    if only and "fp32_1e8_reduce_then_scan" not in only:
+    # The comparison variants on the headline workload: reduce-then-scan (3n element
+    # transfers) and scan-then-fan (4n), each three launches.
+    comparators = [("fp32_1e8_reduce_then_scan", gb.scan_reduce_then_scan, "3n"),
+                   ("fp32_1e8_scan_then_fan", gb.scan_then_fan, "4n")]
+    if only and not any(c[0] in only for c in comparators):
         return out
-    # The reduce-then-scan comparison variant on the headline workload.
     xh = torch.from_numpy(W.BY_NAME[HEADLINE].make()).to(device)
     yh = torch.empty_like(xh)
-    fn = lambda: gb.scan_reduce_then_scan(xh, out=yh)  # noqa: E731
-    for _ in range(3):
-        fn()
-    t = time_call(fn, reps, None, stream, kernel_events=False)
-    ms = t["kernel_ms_best"]
-    out["fp32_1e8_reduce_then_scan"] = {
-        "step_us_best": round(ms * 1e3, 2), "step_us_median": round(t["kernel_ms_median"] * 1e3, 2),
-        "GB_s": round(BYTES_HEAD / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(BYTES_HEAD / (ms * 1e-3) / 1e9 / hbm_peak, 4),
-        "algorithmic_bytes": BYTES_HEAD, "note": "three launches; 2n-byte model, so 3n traffic shows as a lower GB/s"}
+    for name, call, traffic in comparators:
+        if only and name not in only:
+            continue
+        fn = lambda: call(xh, out=yh)  # noqa: E731
+        for _ in range(3):
+            fn()
+        t = time_call(fn, reps, None, stream, kernel_events=False)
+        ms = t["kernel_ms_best"]
+        out[name] = {
+            "step_us_best": round(ms * 1e3, 2), "step_us_median": round(t["kernel_ms_median"] * 1e3, 2),
+            "GB_s": round(BYTES_HEAD / (ms * 1e-3) / 1e9, 1),
+            "frac_hbm": round(BYTES_HEAD / (ms * 1e-3) / 1e9 / hbm_peak, 4), "algorithmic_bytes": BYTES_HEAD,
+            "note": "three launches; 2n-byte model, so %s traffic shows as a lower GB/s" % traffic}
     return out
 
 

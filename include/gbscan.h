@@ -197,6 +197,17 @@ int gb_scan_reduce_then_scan(int dtype, int op, int inclusive, const void* in, v
                              void* stream);
 
 /*
+ * The scan-then-fan comparison variant ([HB] 13.3.2): the same C blocks each scan
+ * their contiguous subarray into `out` and record its total, one block scans the C
+ * totals, then every block after the first combines its base into its outputs (the
+ * fan).  Three launches, 4n element transfers.  lanes = 1.  Same results and errors
+ * as the single-pass scans; temp kind GB_KIND_REDUCE_THEN_SCAN (the same scratch).
+ * `in` and `out` may be the same array.
+ */
+int gb_scan_then_fan(int dtype, int op, int inclusive, const void* in, void* out, int64_t n,
+                     const void* init, void* temp, size_t temp_bytes, void* stream);
+
+/*
  * Inclusive scan of a HOST array into a host array (lanes = 1): the library copies
  * the input to the device, scans it and copies the result back, chunk by chunk, so
  * that the copy of one chunk in and of another out overlap the scan of a third

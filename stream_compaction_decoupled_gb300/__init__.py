@@ -39,6 +39,7 @@ SIGNATURES = {
     "gb_partition": (_i, [_i, _vp, _i64, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "gb_pack_by_counts": (_i, [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "gb_scan_reduce_then_scan": (_i, [_i, _i, _i, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "gb_scan_then_fan": (_i, [_i, _i, _i, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "gb_temp_storage_bytes": (_sz, [_i, _i, _i, _i64, _i64]),
     "gb_device_error": (_i, [_vp]),
     "gb_status_string": (ctypes.c_char_p, [_i]),
@@ -309,3 +310,18 @@ def set_wait_limit_ns(ns: int):
 
 def set_stalled_tile(tile: int):
     load().gb_set_stalled_tile(tile)
+
+
+def scan_then_fan(x, op: str = "add", inclusive: bool = True, init=None, out=None, temp=None, stream=None):
+    """The three-launch scan-then-fan variant (same results as the single-pass scans)."""
+    import torch
+    out = torch.empty_like(x) if out is None else out
+    _need_cuda(x, out)
+    code, n = dtype_code(x.dtype), x.numel()
+    keep, ip = _host_value(code, init, 1)
+    tp, tb = _temp(x, KIND_REDUCE_THEN_SCAN, code, 1, n, 0, temp)
+    _check(load().gb_scan_then_fan(code, OPS[op], 1 if inclusive else 0, ctypes.c_void_p(x.data_ptr()),
+                                   ctypes.c_void_p(out.data_ptr()), n, ip, tp, tb, _stream(x, stream)),
+           "gb_scan_then_fan")
+    del keep
+    return out

@@ -277,6 +277,40 @@ HostLayout host_layout(int dtype, long long chunk) {
   return L;
 }
 
+// The reduce-then-scan (stf = 0) and scan-then-fan (stf = 1) comparators.
+int run_comparator(int stf, int dtype, int op, int inclusive, const void* in, void* out, int64_t n,
+                   const void* init, void* temp, size_t temp_bytes, void* stream) {
+  if (!dtype_size(dtype) || !valid_op(op) || n < 0) return GB_ERR_INVALID;
+  if (!inclusive && !init && !has_identity(op)) return GB_ERR_NO_IDENTITY;
+  if (n == 0) return GB_OK;
+  if (!in || !out) return GB_ERR_INVALID;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  const size_t need = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::rts_temp_bytes<T>(n, ctx.num_sms);
+  });
+  Temp t;
+  rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
+  if (rc) return rc;
+  const std::vector<unsigned char> neutral = identity_bytes(dtype, op, 1);
+  gbs::RtsJob job;
+  job.op = op;
+  job.inclusive = inclusive ? 1 : 0;
+  job.in = in;
+  job.out = out;
+  job.n = n;
+  job.init_host = init ? init : neutral.data();
+  job.temp = t.p;
+  job.scan_then_fan = stf;
+  const cudaError_t e = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::launch_rts<T>(job, ctx);
+  });
+  return e == cudaSuccess ? GB_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -487,37 +521,16 @@ int gb_pack_by_counts(const int32_t* counts, int64_t n, int32_t* offsets, int32_
   return e == cudaSuccess ? GB_OK : cuda_fail(e);
 }
 
+int gb_scan_then_fan(int dtype, int op, int inclusive, const void* in, void* out, int64_t n,
+                     const void* init, void* temp, size_t temp_bytes, void* stream) {
+  return run_comparator(1, dtype, op, inclusive, in, out, n, init, temp, temp_bytes, stream);
+}
+
 int gb_scan_reduce_then_scan(int dtype, int op, int inclusive, const void* in, void* out, int64_t n,
                              const void* init, void* temp, size_t temp_bytes, void* stream) {
-  if (!dtype_size(dtype) || !valid_op(op) || n < 0) return GB_ERR_INVALID;
-  if (!inclusive && !init && !has_identity(op)) return GB_ERR_NO_IDENTITY;
-  if (n == 0) return GB_OK;
-  if (!in || !out) return GB_ERR_INVALID;
-  LaunchCtx ctx;
-  int rc = make_ctx(stream, ctx);
-  if (rc) return rc;
-  const size_t need = with_type(dtype, [&](auto* tp) {
-    using T = std::remove_pointer_t<decltype(tp)>;
-    return gbs::rts_temp_bytes<T>(n, ctx.num_sms);
-  });
-  Temp t;
-  rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
-  if (rc) return rc;
-  const std::vector<unsigned char> neutral = identity_bytes(dtype, op, 1);
-  gbs::RtsJob job;
-  job.op = op;
-  job.inclusive = inclusive ? 1 : 0;
-  job.in = in;
-  job.out = out;
-  job.n = n;
-  job.init_host = init ? init : neutral.data();
-  job.temp = t.p;
-  const cudaError_t e = with_type(dtype, [&](auto* tp) {
-    using T = std::remove_pointer_t<decltype(tp)>;
-    return gbs::launch_rts<T>(job, ctx);
-  });
-  return e == cudaSuccess ? GB_OK : cuda_fail(e);
+  return run_comparator(0, dtype, op, inclusive, in, out, n, init, temp, temp_bytes, stream);
 }
+
 
 size_t gb_temp_storage_bytes(int kind, int dtype, int lanes, int64_t rows, int64_t cols) {
   if (!dtype_size(dtype) || lanes < 1 || lanes > kMaxLanes || rows < 0 || cols < 0) return 0;

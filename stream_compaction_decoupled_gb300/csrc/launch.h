@@ -77,6 +77,7 @@ struct RtsJob {
   long long n = 0;
   const void* init_host = nullptr;
   void* temp = nullptr;
+  int scan_then_fan = 0;  // 0: reduce-then-scan, 1: scan-then-fan
 };
 
 // Each returns a cudaError_t (cudaSuccess on success).  Defined in scan_rows.cuh /

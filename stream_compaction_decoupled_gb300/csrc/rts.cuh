@@ -11,6 +11,17 @@
 // against the single-pass kernel's 2n.  The reduction in launch 1 visits the
 // elements in a strided order, which is fine for the operators provided (all
 // commutative); launch 3 keeps scan order.
+//
+// The scan-then-fan variant (The CUDA Handbook, 13.3.2) uses the same blocks:
+//   launch 1  each block scans its subarray (tile by tile, carrying its own running
+//             total) and writes its total to the partials     (reads n, writes n)
+//   launch 2  one block scans the C partials into exclusive bases
+//   launch 3  each block but the first combines its base into its outputs (fan)
+//                                                            (reads n, writes n)
+// 4n element transfers.  An exclusive scan seeds every block's local scan with the
+// initial value (0 for add, 1 for multiply when none is given; max and min take it
+// more than once harmlessly, being idempotent), so the fan is one combine per
+// element for both kinds.
 #pragma once
 
 #include "launch.h"
@@ -127,7 +138,7 @@ __global__ void __launch_bounds__(kRtsMaxBlocks) rts_spine_kernel(T* partials, i
   if (tid > 0 && tid < nb) partials[tid] = s_incl[tid - 1];  // exclusive base of block tid
 }
 
-template <class T, int OP>
+template <class T, int OP, bool STF>
 __global__ void __launch_bounds__(RowsGeom<T>::NT) rts_scan_kernel(RtsArgs<T> a) {
   pdl_entry();
   using G = RowsGeom<T>;
@@ -141,13 +152,16 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT) rts_scan_kernel(RtsArgs<T> a)
   const long long end = begin + a.per_block < a.n ? begin + a.per_block : a.n;
   const long long ntiles = (end - begin + TILE - 1) / TILE;
 
-  // Carry-in: the block's base (block 0 has none), behind the initial value.
-  bool has = blockIdx.x > 0;
+  // Carry-in: the block's base (block 0 has none; scan-then-fan: none yet), behind
+  // the initial value.  Scan-then-fan also keeps the block's own total.
+  bool has = !STF && blockIdx.x > 0;
   T carry = has ? a.partials[blockIdx.x] : T{};
   if (!a.inclusive) {
     carry = has ? Op<T, OP>::f(a.init, carry) : a.init;
     has = true;
   }
+  T total{};
+  bool htotal = false;
 
   auto tile_len = [&](long long k) -> int {
     const long long s = begin + k * TILE;
@@ -210,6 +224,10 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT) rts_scan_kernel(RtsArgs<T> a)
     const T agg = s_warp[NW - 1];
     carry = has ? Op<T, OP>::f(carry, agg) : agg;
     has = true;
+    if (STF) {
+      total = htotal ? Op<T, OP>::f(total, agg) : agg;
+      htotal = true;
+    }
     if (bulk) {
       fence_proxy_async_smem();
       __syncthreads();
@@ -223,7 +241,42 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT) rts_scan_kernel(RtsArgs<T> a)
     }
     __syncthreads();  // s_warp and the buffer are reused by the next tile
   }
-  if (tid == 0) bulk_wait_read_all();
+  if (tid == 0) {
+    bulk_wait_read_all();
+    if (STF) a.partials[blockIdx.x] = total;
+  }
+}
+
+// Scan-then-fan, launch 3: block b > 0 combines its exclusive base into each of its
+// outputs, on the left (16-byte vectors when aligned, U in flight per thread).
+template <class T, int OP>
+__global__ void __launch_bounds__(256) stf_fan_kernel(RtsArgs<T> a) {
+  pdl_entry();
+  if (blockIdx.x == 0) return;
+  constexpr int NT = 256, VEC = Vec<T>::N, U = 4;
+  const long long begin = (long long)blockIdx.x * a.per_block;
+  const long long end = begin + a.per_block < a.n ? begin + a.per_block : a.n;
+  const T base = a.partials[blockIdx.x];
+  long long i = begin + (long long)threadIdx.x * VEC;
+  if (a.vec_ok) {
+    for (; i + (long long)(U - 1) * NT * VEC + VEC <= end; i += (long long)U * NT * VEC) {
+      Vec<T> x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) x[u] = ld_vec<T>(reinterpret_cast<const uint4*>(a.out + i + (long long)u * NT * VEC));
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) x[u].v[e] = Op<T, OP>::f(base, x[u].v[e]);
+        uint4 w;
+        memcpy(&w, x[u].v, 16);
+        *reinterpret_cast<uint4*>(a.out + i + (long long)u * NT * VEC) = w;
+      }
+    }
+    for (; i < end; i += (long long)NT * VEC)
+      for (long long k = i; k < end && k < i + VEC; ++k) a.out[k] = Op<T, OP>::f(base, a.out[k]);
+  } else {
+    for (long long k = begin + threadIdx.x; k < end; k += NT) a.out[k] = Op<T, OP>::f(base, a.out[k]);
+  }
 }
 
 template <class T> size_t rts_temp_bytes(long long, int) {
@@ -257,12 +310,50 @@ template <class T, int OP> cudaError_t launch_rts_op(const RtsJob& job, const La
   cudaError_t e = launch_pdl(rts_reduce_kernel<T, OP>, a.nblocks, 256, 0, ctx.stream, a);
   if (e == cudaSuccess)
     e = launch_pdl(rts_spine_kernel<T, OP>, 1, kRtsMaxBlocks, 0, ctx.stream, a.partials, a.nblocks);
-  if (e == cudaSuccess) e = launch_pdl(rts_scan_kernel<T, OP>, a.nblocks, RowsGeom<T>::NT, 0, ctx.stream, a);
+  if (e == cudaSuccess) e = launch_pdl(rts_scan_kernel<T, OP, false>, a.nblocks, RowsGeom<T>::NT, 0, ctx.stream, a);
+  profile_after(ctx);
+  return e;
+}
+
+template <class T, int OP> cudaError_t launch_stf_op(const RtsJob& job, const LaunchCtx& ctx) {
+  constexpr int TILE = RowsGeom<T>::TILE;
+  RtsArgs<T> a;
+  a.in = (const T*)job.in;
+  a.out = (T*)job.out;
+  a.n = job.n;
+  const long long tiles = (job.n + TILE - 1) / TILE;
+  long long c = (long long)ctx.num_sms * 6;
+  if (c > kRtsMaxBlocks) c = kRtsMaxBlocks;
+  if (c > tiles) c = tiles;
+  if (c < 1) c = 1;
+  const long long tiles_per_block = (tiles + c - 1) / c;
+  a.per_block = tiles_per_block * TILE;
+  a.nblocks = (int)((job.n + a.per_block - 1) / a.per_block);
+  a.partials = (T*)((char*)job.temp + kHeaderBytes);
+  a.init = T{};
+  if (!job.inclusive && job.init_host) memcpy(&a.init, job.init_host, sizeof(T));
+  a.inclusive = job.inclusive;
+  a.vec_ok = ((uintptr_t)job.in % 16 == 0) && ((uintptr_t)job.out % 16 == 0);
+  a.err = ctx.err;
+  a.wait_ns = ctx.wait_ns;
+  profile_before(ctx);
+  cudaError_t e = launch_pdl(rts_scan_kernel<T, OP, true>, a.nblocks, RowsGeom<T>::NT, 0, ctx.stream, a);
+  if (e == cudaSuccess)
+    e = launch_pdl(rts_spine_kernel<T, OP>, 1, kRtsMaxBlocks, 0, ctx.stream, a.partials, a.nblocks);
+  if (e == cudaSuccess) e = launch_pdl(stf_fan_kernel<T, OP>, a.nblocks, 256, 0, ctx.stream, a);
   profile_after(ctx);
   return e;
 }
 
 template <class T> cudaError_t launch_rts(const RtsJob& job, const LaunchCtx& ctx) {
+  if (job.scan_then_fan) {
+    switch (job.op) {
+      case OP_ADD: return launch_stf_op<T, OP_ADD>(job, ctx);
+      case OP_MAX: return launch_stf_op<T, OP_MAX>(job, ctx);
+      case OP_MUL: return launch_stf_op<T, OP_MUL>(job, ctx);
+      default: return launch_stf_op<T, OP_MIN>(job, ctx);
+    }
+  }
   switch (job.op) {
     case OP_ADD: return launch_rts_op<T, OP_ADD>(job, ctx);
     case OP_MAX: return launch_rts_op<T, OP_MAX>(job, ctx);

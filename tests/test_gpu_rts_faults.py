@@ -41,6 +41,40 @@ def test_rts_matches(dt, op, n):
     assert_scan_matches(got, as3(x, 1, n, 1), op, False, init, what="rts excl")
 
 
+@pytest.mark.parametrize("dt", [np.int32, np.float32, np.float64, np.int64, np.uint32])
+@pytest.mark.parametrize("op", ["add", "max", "min", "mul"])
+@pytest.mark.parametrize("n", [1, 100, 4097, 3 * 4096 + 77, 1_000_003, 12_000_001])
+def test_scan_then_fan_matches(dt, op, n):
+    """Scan-then-fan ([HB] 13.3.2): per-block scans, a scan of the block totals, the fan."""
+    if dt == np.uint32 and not hasattr(torch, "uint32"):
+        pytest.skip("no torch uint32")
+    if op == "mul":
+        x = (workloads.signs_pow2(n, dt, n) if np.dtype(dt).kind == "f"
+             else workloads.odd_ints(n, n, np.int64).astype(dt))
+    else:
+        x = (workloads.normal(n, dt, n) if np.dtype(dt).kind == "f"
+             else workloads.small_ints(n, n, 0 if np.dtype(dt).kind == "u" else -1000, 1000, dtype=dt))
+    xd = dev(x)
+    got = gb.scan_then_fan(xd, op).cpu().numpy()
+    assert_scan_matches(got, as3(x, 1, n, 1), op, True, what="stf %s %s %d" % (np.dtype(dt).name, op, n))
+    init = x[0] if op in ("max", "min") else (x[1 % n] if op == "add" else None)
+    got = gb.scan_then_fan(xd, op, inclusive=False, init=init).cpu().numpy()
+    assert_scan_matches(got, as3(x, 1, n, 1), op, False, init, what="stf excl %s %s" % (op, n))
+    if n > 1:  # in place, through an unaligned view
+        y = dev(np.concatenate([x[:1], x]))[1:]
+        gb.scan_then_fan(y, op, out=y)
+        assert_scan_matches(y.cpu().numpy(), as3(x, 1, n, 1), op, True, what="stf in place %s" % op)
+    assert gb.device_error() == gb.OK
+
+
+def test_scan_then_fan_full_size():
+    w = workloads.BY_NAME["fp32_1e8"]
+    x = w.make()
+    got = gb.scan_then_fan(dev(x)).cpu().numpy()
+    assert_scan_matches(got, as3(x, 1, x.size, 1), "add", True, what="stf fp32 1e8")
+    assert gb.device_error() == gb.OK
+
+
 def test_rts_full_size_matches_single_pass():
     w = workloads.BY_NAME["fp32_1e8"]
     x = w.make()
