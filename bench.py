@@ -71,6 +71,7 @@ KERNEL_SOURCES = {
     "pack_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "pack.cu"),
     "rts_scan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "rts.cuh"),
     "stf_fan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "rts.cuh"),
+    "scan_segmented_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "segmented.cuh"),
     "lanes_rts_reduce_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
     "lanes_rts_spine_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
     "lanes_rts_scan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
@@ -273,6 +274,12 @@ def workload_call(w, device):
         torch.cuda.synchronize()
         m = int(cnt.item())
         return fn, 4 * x.numel() + 4 * m + 4, x.numel(), "Gelem/s"
+    if w.kind == "segmented":  # values, one head flag byte per element, values out
+        from stream_compaction_decoupled_gb300.workloads import head_flags
+        fl = torch.from_numpy(head_flags(x.numel(), w.extra["p_head"], w.extra["flag_seed"])).to(device)
+        y = torch.empty_like(x)
+        fn = lambda: gb.scan_segmented(x, fl, w.op, out=y)  # noqa: E731
+        return fn, 2 * x.numel() * es + x.numel(), x.numel(), "Gelem/s"
     if w.kind == "partition":  # values and their input indices
         out = torch.empty_like(x)
         idx = torch.empty(x.numel(), dtype=torch.int32, device=device)

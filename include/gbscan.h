@@ -86,7 +86,8 @@ enum gb_kind {
   GB_KIND_COMPACT = 3,       /* gb_compact: rows = n                                  */
   GB_KIND_PACK = 4,          /* gb_pack_by_counts: rows = n                           */
   GB_KIND_REDUCE_THEN_SCAN = 5, /* gb_scan_reduce_then_scan: rows = n                 */
-  GB_KIND_PARTITION = 6        /* gb_partition: rows = n                              */
+  GB_KIND_PARTITION = 6,       /* gb_partition: rows = n                              */
+  GB_KIND_SEGMENTED = 7        /* gb_scan_segmented: rows = n                         */
 };
 
 /* Status codes. */
@@ -168,6 +169,20 @@ int gb_compact(int dtype, const void* in, int64_t n, int pred, const void* thres
  */
 int gb_partition(int dtype, const void* in, int64_t n, int pred, const void* threshold, void* out,
                  int32_t* out_idx, int32_t* out_count, void* temp, size_t temp_bytes, void* stream);
+
+/*
+ * Segmented scan by head flags (lanes = 1): flags[i] != 0 marks element i as the
+ * first of a segment (element 0 always is one), and every segment is scanned on its
+ * own: inclusive  out_i = x_h (+) ... (+) x_i,  exclusive  out_i = init (+) x_h (+)
+ * ... (+) x_{i-1}  (out_h = init), h the last head at or before i.  The segmented
+ * operator on (value, flag) pairs is associative but not commutative ([HB] 13.3.4's
+ * caveat on the packed descriptor), and the kernel combines in index order
+ * throughout.  flags: n bytes (device).  init as in gb_scan_exclusive (NULL: 0 for
+ * ADD, 1 for MUL; required for MAX / MIN).  in == out is allowed.  temp kind:
+ * GB_KIND_SEGMENTED.
+ */
+int gb_scan_segmented(int dtype, int op, int inclusive, const void* in, const uint8_t* flags, void* out,
+                      int64_t n, const void* init, void* temp, size_t temp_bytes, void* stream);
 
 /*
  * Variable-length packing ([PS] "Output Format" and "Solution"): object i emits

@@ -51,6 +51,8 @@ def _load():
         lib.oracle_scan.restype = i
         lib.oracle_compact.argtypes = [i, vp, i64, i, vp, vp]
         lib.oracle_compact.restype = i64
+        lib.oracle_scan_segmented.argtypes = [i, i, i, vp, vp, vp, i64, vp]
+        lib.oracle_scan_segmented.restype = i
         lib.oracle_partition.argtypes = [i, vp, i64, i, vp, vp, vp]
         lib.oracle_partition.restype = i64
         lib.oracle_pack_by_counts.argtypes = [vp, i64, vp, vp, i64]
@@ -132,6 +134,27 @@ def compact(x: np.ndarray, pred: str, threshold) -> np.ndarray:
     if cnt < 0:
         raise ValueError("oracle_compact rejected its arguments (%d)" % cnt)
     return out[:cnt].copy()
+
+
+def scan_segmented(x: np.ndarray, flags: np.ndarray, op: str = "add", inclusive: bool = True,
+                   init=None) -> np.ndarray:
+    """Scan restarting at head flags (flags[i] != 0: element i starts a segment;
+    element 0 always does).  Integers keep their type; floats give fp64."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    fl = np.ascontiguousarray(flags, dtype=np.uint8).reshape(-1)
+    if fl.size != x.size:
+        raise ValueError("one flag per element")
+    dt = dtype_name(x)
+    out = np.empty(max(x.size, 1), dtype=np.float64 if dt in ("f32", "f64") else x.dtype)
+    ia = None if init is None else np.asarray(init, dtype=x.dtype).reshape(1)
+    rc = _load().oracle_scan_segmented(_DTYPES[dt], _OPS[op], 1 if inclusive else 0, x.ctypes.data,
+                                       fl.ctypes.data, out.ctypes.data, x.size,
+                                       None if ia is None else ia.ctypes.data)
+    if rc == -2:
+        raise NoIdentity("exclusive %s scan needs an initial value" % op)
+    if rc != 0:
+        raise ValueError("oracle_scan_segmented rejected its arguments (%d)" % rc)
+    return out[:x.size].copy()
 
 
 def partition(x: np.ndarray, pred: str, threshold):

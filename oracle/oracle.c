@@ -293,6 +293,67 @@ int64_t oracle_compact(int dtype, const void *in, int64_t n, int pred,
     return count;
 }
 
+/* ---- segmented scans -------------------------------------------------------- */
+
+/*
+ * Scan restarting at head flags: flags[i] != 0 marks element i as the first of a
+ * segment (element 0 always is one).  Inclusive out_i = x_h (+) ... (+) x_i;
+ * exclusive out_i = init (+) x_h (+) ... (+) x_{i-1}, out_h = init; h the last
+ * head at or before i.  One left-to-right loop that forgets its running value at
+ * every head.  Outputs and init typing as for oracle_scan (floats: fp64).
+ */
+int oracle_scan_segmented(int dtype, int op, int inclusive, const void *in,
+                          const uint8_t *flags, void *out, int64_t n,
+                          const void *init)
+{
+    if (n < 0 || dtype < OR_I32 || dtype > OR_F64) return OR_BAD_ARGUMENT;
+    if (op != OR_ADD && op != OR_MAX && op != OR_MIN && op != OR_MUL) return OR_BAD_ARGUMENT;
+    if (!inclusive && (op == OR_MAX || op == OR_MIN) && !init) return OR_NO_IDENTITY;
+    int is_fp = dtype == OR_F32 || dtype == OR_F64;
+    int is_signed = dtype == OR_I32 || dtype == OR_I64;
+    int wide = dtype == OR_I64 || dtype == OR_U64;
+    uint64_t iacc = 0, iinit = op == OR_MUL ? 1u : 0u;
+    double facc = 0.0, finit = op == OR_MUL ? 1.0 : 0.0;
+    if (init) {
+        switch (dtype) {
+        case OR_I32: iinit = (uint32_t)*(const int32_t *)init; break;
+        case OR_U32: iinit = *(const uint32_t *)init; break;
+        case OR_I64: case OR_U64: iinit = *(const uint64_t *)init; break;
+        case OR_F32: finit = *(const float *)init; break;
+        default: finit = *(const double *)init; break;
+        }
+    }
+    for (int64_t i = 0; i < n; i++) {
+        int head = i == 0 || flags[i] != 0;
+        double fx = 0.0;
+        uint64_t ix = 0;
+        switch (dtype) {
+        case OR_I32: ix = (uint32_t)((const int32_t *)in)[i]; break;
+        case OR_U32: ix = ((const uint32_t *)in)[i]; break;
+        case OR_I64: case OR_U64: ix = ((const uint64_t *)in)[i]; break;
+        case OR_F32: fx = ((const float *)in)[i]; break;
+        default: fx = ((const double *)in)[i]; break;
+        }
+        if (is_fp) {
+            if (!inclusive) ((double *)out)[i] = head ? finit : op_f64(op, finit, facc);
+            facc = head ? fx : op_f64(op, facc, fx);
+            if (inclusive) ((double *)out)[i] = facc;
+        } else if (!wide) {
+            uint32_t a = (uint32_t)iacc, x = (uint32_t)ix, t = (uint32_t)iinit;
+            uint32_t e = head ? t : (is_signed ? op_u32bits_signed(op, t, a) : op_u32bits_unsigned(op, t, a));
+            a = head ? x : (is_signed ? op_u32bits_signed(op, a, x) : op_u32bits_unsigned(op, a, x));
+            ((uint32_t *)out)[i] = inclusive ? a : e;
+            iacc = a;
+        } else {
+            uint64_t e = head ? iinit : (is_signed ? op_u64bits_signed(op, iinit, iacc)
+                                                   : op_u64bits_unsigned(op, iinit, iacc));
+            iacc = head ? ix : (is_signed ? op_u64bits_signed(op, iacc, ix) : op_u64bits_unsigned(op, iacc, ix));
+            ((uint64_t *)out)[i] = inclusive ? iacc : e;
+        }
+    }
+    return OR_OK;
+}
+
 /* ---- partition ----------------------------------------------------------- */
 
 /* Is bit b of the element's bit pattern clear?  (Integer types.) */

@@ -22,7 +22,7 @@ I32, U32, I64, U64, F32, F64 = range(6)
 ADD, MAX, MIN, MUL = range(4)
 LT, LE, GT, GE, EQ, NE, BIT_CLEAR = range(7)
 KIND_SCAN, KIND_BATCHED_AXIS1, KIND_BATCHED_AXIS0, KIND_COMPACT, KIND_PACK, KIND_REDUCE_THEN_SCAN, \
-    KIND_PARTITION = range(7)
+    KIND_PARTITION, KIND_SEGMENTED = range(8)
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_TEMP, ERR_NO_IDENTITY, ERR_RANGE, ERR_CUDA, ERR_TIMEOUT = range(8)
 
 OPS = {"add": ADD, "max": MAX, "min": MIN, "mul": MUL}
@@ -40,6 +40,7 @@ SIGNATURES = {
     "gb_pack_by_counts": (_i, [_vp, _i64, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "gb_scan_reduce_then_scan": (_i, [_i, _i, _i, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "gb_scan_then_fan": (_i, [_i, _i, _i, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
+    "gb_scan_segmented": (_i, [_i, _i, _i, _vp, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "gb_temp_storage_bytes": (_sz, [_i, _i, _i, _i64, _i64]),
     "gb_device_error": (_i, [_vp]),
     "gb_status_string": (ctypes.c_char_p, [_i]),
@@ -323,5 +324,25 @@ def scan_then_fan(x, op: str = "add", inclusive: bool = True, init=None, out=Non
     _check(load().gb_scan_then_fan(code, OPS[op], 1 if inclusive else 0, ctypes.c_void_p(x.data_ptr()),
                                    ctypes.c_void_p(out.data_ptr()), n, ip, tp, tb, _stream(x, stream)),
            "gb_scan_then_fan")
+    del keep
+    return out
+
+
+def scan_segmented(x, flags, op: str = "add", inclusive: bool = True, init=None, out=None, temp=None, stream=None):
+    """Segmented scan: flags (uint8 or bool, same length) marks the first element of
+    each segment; every segment is scanned on its own (element 0 always starts one)."""
+    import torch
+    out = torch.empty_like(x) if out is None else out
+    if flags.dtype == torch.bool:
+        flags = flags.view(torch.uint8)
+    if flags.dtype != torch.uint8 or flags.numel() != x.numel() or not flags.is_contiguous():
+        raise ValueError("flags must be a contiguous uint8 (or bool) tensor with one entry per element")
+    _need_cuda(x, out, flags)
+    code, n = dtype_code(x.dtype), x.numel()
+    keep, ip = _host_value(code, init, 1)
+    tp, tb = _temp(x, KIND_SEGMENTED, code, 1, n, 0, temp)
+    _check(load().gb_scan_segmented(code, OPS[op], 1 if inclusive else 0, ctypes.c_void_p(x.data_ptr()),
+                                    ctypes.c_void_p(flags.data_ptr()), ctypes.c_void_p(out.data_ptr()), n, ip,
+                                    tp, tb, _stream(x, stream)), "gb_scan_segmented")
     del keep
     return out

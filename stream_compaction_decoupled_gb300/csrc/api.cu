@@ -493,6 +493,39 @@ int gb_partition(int dtype, const void* in, int64_t n, int pred, const void* thr
   return e == cudaSuccess ? GB_OK : cuda_fail(e);
 }
 
+int gb_scan_segmented(int dtype, int op, int inclusive, const void* in, const uint8_t* flags, void* out,
+                      int64_t n, const void* init, void* temp, size_t temp_bytes, void* stream) {
+  if (!dtype_size(dtype) || !valid_op(op) || n < 0) return GB_ERR_INVALID;
+  if (!inclusive && !init && !has_identity(op)) return GB_ERR_NO_IDENTITY;
+  if (n == 0) return GB_OK;
+  if (!in || !out || !flags) return GB_ERR_INVALID;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  const size_t need = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::segmented_temp_bytes<T>();
+  });
+  Temp t;
+  rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
+  if (rc) return rc;
+  const std::vector<unsigned char> neutral = identity_bytes(dtype, op, 1);
+  gbs::SegmentedJob job;
+  job.op = op;
+  job.inclusive = inclusive ? 1 : 0;
+  job.in = in;
+  job.flags = flags;
+  job.out = out;
+  job.n = n;
+  job.init_host = init ? init : neutral.data();
+  job.temp = t.p;
+  const cudaError_t e = with_type(dtype, [&](auto* tp) {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    return gbs::launch_segmented<T>(job, ctx);
+  });
+  return e == cudaSuccess ? GB_OK : cuda_fail(e);
+}
+
 int gb_pack_by_counts(const int32_t* counts, int64_t n, int32_t* offsets, int32_t* out_records,
                       int64_t out_capacity, int32_t* out_total, void* temp, size_t temp_bytes, void* stream) {
   if (n < 0 || out_capacity < 0 || !out_total) return GB_ERR_INVALID;
@@ -552,6 +585,11 @@ size_t gb_temp_storage_bytes(int kind, int dtype, int lanes, int64_t rows, int64
       return with_type(dtype, [&](auto* tp) {
         using T = std::remove_pointer_t<decltype(tp)>;
         return gbs::partition_temp_bytes<T>();
+      });
+    case GB_KIND_SEGMENTED:
+      return with_type(dtype, [&](auto* tp) {
+        using T = std::remove_pointer_t<decltype(tp)>;
+        return gbs::segmented_temp_bytes<T>();
       });
     case GB_KIND_REDUCE_THEN_SCAN:
       return with_type(dtype, [&](auto* tp) {

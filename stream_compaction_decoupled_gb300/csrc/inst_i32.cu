@@ -2,6 +2,7 @@
 // element type, so the library builds in parallel).
 #include "compact.cuh"
 #include "partition.cuh"
+#include "segmented.cuh"
 #include "rts.cuh"
 #include "scan.cuh"
 

@@ -59,6 +59,17 @@ struct PartitionJob {
   void* temp = nullptr;
 };
 
+struct SegmentedJob {
+  int op = 0;
+  int inclusive = 1;
+  const void* in = nullptr;
+  const void* flags = nullptr;  // n bytes, nonzero = head
+  void* out = nullptr;
+  long long n = 0;
+  const void* init_host = nullptr;  // exclusive: the value each segment starts from
+  void* temp = nullptr;
+};
+
 struct PackJob {
   const int32_t* counts = nullptr;
   long long n = 0;
@@ -88,6 +99,8 @@ template <class T> size_t compact_temp_bytes(long long n);
 template <class T> cudaError_t launch_compact(const CompactJob& job, const LaunchCtx& ctx);
 template <class T> size_t partition_temp_bytes();
 template <class T> cudaError_t launch_partition(const PartitionJob& job, const LaunchCtx& ctx);
+template <class T> size_t segmented_temp_bytes();
+template <class T> cudaError_t launch_segmented(const SegmentedJob& job, const LaunchCtx& ctx);
 template <class T> size_t rts_temp_bytes(long long n, int num_sms);
 template <class T> cudaError_t launch_rts(const RtsJob& job, const LaunchCtx& ctx);
 size_t pack_temp_bytes(long long n);

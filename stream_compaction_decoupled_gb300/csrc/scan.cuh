@@ -95,6 +95,8 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
   template cudaError_t launch_compact<T>(const CompactJob&, const LaunchCtx&);              \
   template size_t partition_temp_bytes<T>();                                                \
   template cudaError_t launch_partition<T>(const PartitionJob&, const LaunchCtx&);          \
+  template size_t segmented_temp_bytes<T>();                                                \
+  template cudaError_t launch_segmented<T>(const SegmentedJob&, const LaunchCtx&);          \
   template size_t rts_temp_bytes<T>(long long, int);                                        \
   template cudaError_t launch_rts<T>(const RtsJob&, const LaunchCtx&);                      \
   }

@@ -65,6 +65,11 @@ def signs_pow2(n: int, dtype, seed: int, span: int = 30) -> np.ndarray:
     return (sign * np.exp2(step)).astype(dtype)
 
 
+def head_flags(n: int, p: float, seed: int) -> np.ndarray:
+    """n uint8 head flags, each 1 with probability p (segments of mean length 1/p)."""
+    return (rng(seed).random(n) < p).astype(np.uint8)
+
+
 def poisson_counts(n: int, lam: float, seed: int) -> np.ndarray:
     """n int32 record counts k_i ~ Poisson(lam)."""
     return rng(seed).poisson(lam, n).astype(np.int32)
@@ -96,7 +101,7 @@ def values(kind: str, n: int, dtype, seed: int, extra: dict | None = None) -> np
 class Workload:
     """One benchmark configuration: what to scan or compact, and its seed."""
     name: str
-    kind: str            # "scan", "batched", "compact", "pack", "partition"
+    kind: str            # "scan", "batched", "compact", "pack", "partition", "segmented"
     dtype: str           # numpy dtype name of one lane
     shape: tuple         # (n,) or (rows, cols)
     dist: str
@@ -151,6 +156,9 @@ WORKLOADS = [
     Workload("struct32_1e6", "scan", "float32", (1_000_000,), "normal", 18, lanes=8),
     Workload("elem2080_2e4", "scan", "float32", (20_000,), "normal", 19, lanes=520),
     Workload("elem2080_2e4_max", "scan", "float32", (20_000,), "normal", 20, lanes=520, op="max"),
+    # Segmented scan by head flags: segments of mean length 1000.
+    Workload("fp32_1e7_segmented", "segmented", "float32", (10_000_000,), "normal", 22,
+             extra={"p_head": 0.001, "flag_seed": 23}),
     # Stable partition (x < 0.5 first) of the compaction input's shape, values and indices.
     Workload("partition_p0.5", "partition", "float32", (10_000_000,), "uniform01", 21, extra={"p": 0.5}),
 ]

@@ -92,7 +92,8 @@ def stall():
 
 
 @pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "lanes_wide", "segments", "segments_f64",
-                                  "compact_segments", "compact_tiles", "pack", "l2_resident", "partition"])
+                                  "compact_segments", "compact_tiles", "pack", "l2_resident", "partition",
+                                  "segmented"])
 def test_stalled_tile_times_out(stall, kind):
     n = 64 * 4096 if kind != "l2_resident" else 26_000_000
     x = workloads.uniform01(n, np.float32, 1)
@@ -114,6 +115,8 @@ def test_stalled_tile_times_out(stall, kind):
         gb.scan_inclusive(dev(x))
     elif kind == "compact_segments":
         gb.compact(dev(x), "lt", 0.5)
+    elif kind == "segmented":  # head-flag scan: segment 3 never publishes its pair
+        gb.scan_segmented(dev(x), dev(workloads.head_flags(n, 0.01, 2)))
     elif kind == "partition":  # every segment waits for all counts; segment 3 never publishes
         gb.partition(dev(x), "lt", 0.5)
     elif kind == "compact_tiles":

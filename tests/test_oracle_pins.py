@@ -436,3 +436,54 @@ def test_partition_special_cases():
         oracle.partition(y, "bit_clear", 32)             # no bit 32 in int32
     with pytest.raises(ValueError):
         oracle.partition(x, "bit_clear", 1)              # floats have no bit split
+
+
+# ------------------------------------------------------------ segmented scan --
+
+def _numpy_segments(x, flags, op, inclusive, init):
+    """Each segment scanned on its own with numpy's accumulate (a library routine)."""
+    heads = np.flatnonzero(flags)
+    heads = np.union1d([0], heads).astype(np.int64)
+    out = []
+    for a, b in zip(heads, list(heads[1:]) + [x.size]):
+        seg = x[a:b]
+        if x.dtype.kind == "f":
+            seg = seg.astype(np.float64)
+        acc = {"add": np.add, "max": np.maximum, "min": np.minimum, "mul": np.multiply}[op].accumulate(seg, dtype=seg.dtype)
+        if inclusive:
+            out.append(acc)
+        else:
+            first = np.asarray([init], dtype=acc.dtype)
+            body = {"add": np.add, "max": np.maximum, "min": np.minimum, "mul": np.multiply}[op](
+                np.asarray(init, dtype=acc.dtype), acc[:-1])
+            out.append(np.concatenate([first, body]))
+    return np.concatenate(out) if out else np.zeros(0, x.dtype)
+
+
+def test_segmented_against_numpy_per_segment():
+    r = np.random.default_rng(63)
+    for dt in (np.int32, np.int64, np.uint32, np.float64):
+        for p in (0.0, 0.01, 0.3, 1.0):
+            x = r.integers(-50 if dt != np.uint32 else 0, 50, 2000).astype(dt)
+            fl = (r.random(2000) < p).astype(np.uint8)
+            for op in ("add", "max", "min", "mul"):
+                got = oracle.scan_segmented(x, fl, op)
+                assert np.array_equal(got, _numpy_segments(x, fl, op, True, None)), (dt, p, op)
+                init = 7 if op in ("add", "mul") else 3
+                got = oracle.scan_segmented(x, fl, op, False, init)
+                assert np.array_equal(got, _numpy_segments(x, fl, op, False, init)), (dt, p, op, "excl")
+
+
+def test_segmented_closed_forms_and_rows():
+    r = np.random.default_rng(64)
+    x = r.integers(-9, 9, 4096).astype(np.int32)
+    assert np.array_equal(oracle.scan_segmented(x, np.ones(4096, np.uint8)), x)          # every element a head
+    assert np.array_equal(oracle.scan_segmented(x, np.ones(4096, np.uint8), inclusive=False), np.zeros(4096))
+    ones = np.ones(5000, np.float32)
+    assert np.array_equal(oracle.scan_segmented(ones, np.zeros(5000, np.uint8)), np.arange(1, 5001))
+    rows = x.reshape(64, 64)                                                             # equal segments = rows
+    fl = np.zeros(4096, np.uint8)
+    fl[::64] = 1
+    assert np.array_equal(oracle.scan_segmented(x, fl).reshape(64, 64), np.cumsum(rows, axis=1, dtype=np.int32))
+    with pytest.raises(oracle.NoIdentity):
+        oracle.scan_segmented(x, fl, "max", inclusive=False)
