@@ -99,18 +99,30 @@ __device__ __forceinline__ void seg_pair_load(const SegmentedArgs<T>& a, long lo
   if (e0 == 0) fl |= 1u;
 }
 
+// A full chunk leaves through the warp's staging buffer (32 lanes x 4 granules of 16
+// bytes): lane l puts its granule q at l*4 + (q ^ ((l >> 1) & 3)), which spreads every
+// 8 lanes over the 8 granule slots of 128 bytes (no bank conflict), then the warp
+// stores the chunk's 2 KB as consecutive 16-byte pieces, whole lines per instruction.
+// A lane's 64-byte stride alone would leave each store instruction half lines.
 template <class T, class G>
 __device__ __forceinline__ void seg_pair_store(const SegmentedArgs<T>& a, long long c, int lane, const T (&y)[G::K],
-                                               unsigned long long pol) {
-  constexpr int K = G::K, CH = G::CH;
+                                               uint4* stage, unsigned long long pol) {
+  constexpr int K = G::K, CH = G::CH, GR = K * (int)sizeof(T) / 16;  // granules per lane: 4
   const long long e0 = c * CH + (long long)lane * K;
   if (a.vec && c * CH + CH <= a.n) {
-    uint4* p = reinterpret_cast<uint4*>(a.out + e0);
+    __syncwarp();  // the previous chunk's stores have read the buffer
 #pragma unroll
-    for (int q = 0; q < K * (int)sizeof(T) / 16; ++q) {
+    for (int q = 0; q < GR; ++q) {
       uint4 u;
       memcpy(&u, &y[q * 16 / sizeof(T)], 16);
-      st_hint(p + q, u, pol);
+      stage[lane * GR + (q ^ ((lane >> 1) & 3))] = u;
+    }
+    __syncwarp();
+    uint4* base = reinterpret_cast<uint4*>(a.out + c * CH);
+#pragma unroll
+    for (int it = 0; it < GR; ++it) {
+      const int g = it * 32 + lane, l = g / GR, q = (g % GR) ^ ((l >> 1) & 3);
+      st_hint(base + l * GR + q, stage[g], pol);
     }
   } else {
 #pragma unroll
@@ -198,7 +210,9 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_segmented_kernel(Segmente
   __shared__ int s_wf[NW];
   __shared__ T s_bv;
   __shared__ int s_bf, s_bhas;
+  __shared__ uint4 s_stage_all[NW * 32 * (K * sizeof(T) / 16)];  // a chunk's outputs per warp
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint4* s_stage = s_stage_all + warp * 32 * (K * sizeof(T) / 16);
   if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
   __syncthreads();
   const unsigned seg = s_seg;
@@ -330,7 +344,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_segmented_kernel(Segmente
       }
       rhas = true;
     }
-    seg_pair_store<T, G>(a, c, lane, y, drop);
+    seg_pair_store<T, G>(a, c, lane, y, s_stage, drop);
   }
 }
 
