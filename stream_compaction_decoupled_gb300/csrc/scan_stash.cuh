@@ -35,12 +35,22 @@
 
 namespace gbs {
 
-// Defaults from a sweep on the fp32 1e8 inclusive scan (kernel time, best of 12):
-// 2 reducers, 1 look-back warp, 3 scanning groups, 4 + 3x3 buffers of 16 KB, runs of
-// 4 tiles, 8 runs queued: 145.7 us.  More warps cost registers (all roles share one
-// register budget, and the scanning warps then spill); a wider look-back window did
-// the same; runs of 8 tiles or a deeper queue pressed L2 harder.
-template <class T, int NR_ = 2, int NG_ = 3, int NL_ = 4, int NS_ = 3, int K_ = 2, int RUN_ = 4, int QD_ = 8,
+// Defaults from sweeps on the fp32 1e8 and 2e8 inclusive scans (per-step time of 20
+// chained calls, best of 5; the same box for every line):
+//   4 load buffers, window 64 runs, runs of 4, 8 queued      140.3 us   265.5 us
+//   5 load buffers, the rest as above                         140.5 us   267.2 us
+//   window of 32 runs, the rest as above                      140.4 us   265.9 us
+//   5 load buffers, window 32, runs of 4, 8 queued            137.0 us   261.5 us
+//   5 load buffers, window 32, runs of 3, 10 queued           134.7 us   255.9 us  <- defaults
+//   ... runs of 3, 8 / 12 queued                              134.7 / 137.8   256.9 / 266.6
+//   ... runs of 2, 14 / 16 queued                             147.1 / 151.6
+//   3 load buffers; 7 or 8 load buffers with 2 per group      155.3; 151.3 / 153.8
+//   two look-back warps on alternate runs                     179.7 us
+// More loads in flight from HBM pay as long as each scanning group keeps 3 re-load
+// buffers; shorter runs halve the wait for a run's prefix but need more runs queued,
+// which presses L2 beyond about 30 queued tiles per SM.  More warps cost registers
+// (all roles share one register budget, and the scanning warps then spill).
+template <class T, int NR_ = 2, int NG_ = 3, int NL_ = 5, int NS_ = 3, int K_ = 1, int RUN_ = 3, int QD_ = 10,
           int NB_ = 1>
 struct StashCfgT {
   static constexpr int VEC = 16 / (int)sizeof(T);

@@ -111,7 +111,7 @@ def test_stalled_tile_times_out(stall, kind):
         gb.scan_inclusive(dev(x[: n // 65 * 65]), lanes=65)
     elif kind == "segments":  # 512 chunks -> 16 segments; segment 3 never publishes
         gb.scan_inclusive(dev(x))
-    elif kind == "l2_resident":  # one long row: the stalled index is a run of 4 tiles
+    elif kind == "l2_resident":  # one long row: the stalled index is a run of tiles
         gb.scan_inclusive(dev(x))
     elif kind == "compact_segments":
         gb.compact(dev(x), "lt", 0.5)
