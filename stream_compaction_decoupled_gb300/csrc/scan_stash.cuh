@@ -41,16 +41,18 @@ namespace gbs {
 //   5 load buffers, the rest as above                         140.5 us   267.2 us
 //   window of 32 runs, the rest as above                      140.4 us   265.9 us
 //   5 load buffers, window 32, runs of 4, 8 queued            137.0 us   261.5 us
-//   5 load buffers, window 32, runs of 3, 10 queued           134.7 us   255.9 us  <- defaults
-//   ... runs of 3, 8 / 12 queued                              134.7 / 137.8   256.9 / 266.6
+//   5 load buffers, window 32, runs of 3, 10 queued           134.7 us   255.9 us
+//   ... runs of 3, 9 queued (three repeats, interleaved)      132.6-133.0  252.0-252.3  <- defaults
+//   ... runs of 3, 8 / 10 / 12 queued                         133.9 / 134.1 / 137.8   255.0 / 255.4 / 266.6
 //   ... runs of 2, 14 / 16 queued                             147.1 / 151.6
-//   3 load buffers; 7 or 8 load buffers with 2 per group      155.3; 151.3 / 153.8
-//   two look-back warps on alternate runs                     179.7 us
+//   3 / 4 load buffers (runs of 4 / 3)                       155.3 / 136.9 us
+//   7 or 8 load buffers with 2 per group; 2 groups of 4       151.3 / 153.8; 143.7 us
+//   1 or 3 reducers; two look-back warps on alternate runs    166.2 / 178.4; 179.7 us
 // More loads in flight from HBM pay as long as each scanning group keeps 3 re-load
 // buffers; shorter runs halve the wait for a run's prefix but need more runs queued,
 // which presses L2 beyond about 30 queued tiles per SM.  More warps cost registers
 // (all roles share one register budget, and the scanning warps then spill).
-template <class T, int NR_ = 2, int NG_ = 3, int NL_ = 5, int NS_ = 3, int K_ = 1, int RUN_ = 3, int QD_ = 10,
+template <class T, int NR_ = 2, int NG_ = 3, int NL_ = 5, int NS_ = 3, int K_ = 1, int RUN_ = 3, int QD_ = 9,
           int NB_ = 1>
 struct StashCfgT {
   static constexpr int VEC = 16 / (int)sizeof(T);
