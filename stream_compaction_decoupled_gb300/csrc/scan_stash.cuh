@@ -48,12 +48,14 @@ namespace gbs {
 //   3 / 4 load buffers (runs of 4 / 3)                       155.3 / 136.9 us
 //   7 or 8 load buffers with 2 per group; 2 groups of 4       151.3 / 153.8; 143.7 us
 //   1 or 3 reducers; two look-back warps on alternate runs    166.2 / 178.4; 179.7 us
+//   12 KB or 8 KB tiles with more buffers (another box: 16 KB 136.9 us there)
+//                                                             137.5-141.9; 165.1 us
 // More loads in flight from HBM pay as long as each scanning group keeps 3 re-load
 // buffers; shorter runs halve the wait for a run's prefix but need more runs queued,
 // which presses L2 beyond about 30 queued tiles per SM.  More warps cost registers
 // (all roles share one register budget, and the scanning warps then spill).
 template <class T, int NR_ = 2, int NG_ = 3, int NL_ = 5, int NS_ = 3, int K_ = 1, int RUN_ = 3, int QD_ = 9,
-          int NB_ = 1>
+          int NB_ = 1, int ROUNDS_ = 8>
 struct StashCfgT {
   static constexpr int VEC = 16 / (int)sizeof(T);
   static constexpr int NR = NR_;                      // reducer warps
@@ -63,8 +65,8 @@ struct StashCfgT {
   static constexpr int WB = 1 + NR;                   // first look-back warp
   static constexpr int WS = WB + NB;                  // first scanning warp
   static constexpr int NT = 32 * (WS + NG * NSW);
-  static constexpr int ROUNDS = 8;                    // S: 16-byte vectors per thread per tile
-  static constexpr int TILE = NSW * ROUNDS * 32 * VEC;  // 16 KB
+  static constexpr int ROUNDS = ROUNDS_;              // S: 16-byte vectors per thread per tile
+  static constexpr int TILE = NSW * ROUNDS * 32 * VEC;  // 16 KB at 8 rounds
   static constexpr int RUN = RUN_;                    // tiles per run (one look-back per run)
   static constexpr int NL = NL_;                      // I/R buffers: bulk loads from HBM in flight
   static constexpr int NS = NS_;                      // buffers per scanning group (re-loads from L2)
