@@ -42,7 +42,7 @@ template <class T> struct LanesArgs {
 // and 1e6x8 axis 0, 96-byte structs, 17-lane duals, 1000x1e4 fp64 axis 0) put 32 at
 // or near the best everywhere: fewer, larger tiles mean fewer look-backs along a
 // chain, which is what limits these scans (dual16 1e6: 372 us at 8, 165 us at 32).
-template <class T, int RPG_ = 32, int D_ = 4> struct LanesGeomT {
+template <class T, int RPG_ = 32, int D_ = 4, int CTMAX_ = 0> struct LanesGeomT {
   static constexpr int NT = 256;
   static constexpr int NW = NT / 32;
   static constexpr int RPG = RPG_;                        // rows per thread
@@ -50,7 +50,10 @@ template <class T, int RPG_ = 32, int D_ = 4> struct LanesGeomT {
   // lane workload measured (96-byte structs 1e6: 51.9 / 59.5 / 62.1 us at 4 / 8 / 16;
   // 17-lane duals 1e6: 162 / 176 / 232 us): wider windows cost registers and occupancy.
   static constexpr int D = D_;
-  static constexpr int CTMAX = sizeof(T) == 4 ? 64 : 32;  // 256-byte strips
+  // Strip width: 256-byte strips.  Wider strips (fewer, larger per-row copies, longer
+  // chains) measured slower everywhere (4096 x 4096 fp32 columns: 43.6 / 49.8 / 62.0 us
+  // at 64 / 128 / 256 lanes; 1000 x 1e4 fp64: 72-74 / 74.3 / 76.4 us at 32 / 64 / 128).
+  static constexpr int CTMAX = CTMAX_ > 0 ? CTMAX_ : (sizeof(T) == 4 ? 64 : 32);
   static int ct(long long C) { return C <= CTMAX ? (int)C : CTMAX; }
   static int groups(int CT) {
     int g = NT / CT;
