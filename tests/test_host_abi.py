@@ -30,8 +30,8 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     for need in ("gb_scan_inclusive", "gb_scan_exclusive", "gb_scan_batched", "gb_compact",
-                 "gb_pack_by_counts", "gb_scan_reduce_then_scan", "gb_temp_storage_bytes",
-                 "gb_device_error", "gb_status_string"):
+                 "gb_partition", "gb_scan_segmented", "gb_pack_by_counts", "gb_scan_reduce_then_scan",
+                 "gb_scan_then_fan", "gb_temp_storage_bytes", "gb_device_error", "gb_status_string"):
         assert need in names
 
 
@@ -50,6 +50,7 @@ def test_c_translation_unit_compiles_against_header(tmp_path):
                  ' size_t t = gb_temp_storage_bytes(GB_KIND_SCAN, GB_F32, 1, 100, 0);\n'
                  ' (void)gb_scan_inclusive; (void)gb_scan_exclusive; (void)gb_scan_batched;\n'
                  ' (void)gb_compact; (void)gb_pack_by_counts; (void)gb_scan_reduce_then_scan;\n'
+                 ' (void)gb_partition; (void)gb_scan_segmented; (void)gb_scan_then_fan;\n'
                  ' (void)gb_device_error; (void)gb_last_cuda_error; (void)gb_set_profile_events;\n'
                  ' (void)gb_set_wait_limit_ns; (void)gb_set_stalled_tile;\n'
                  ' return t > 0 && gb_version() > 0 ? 0 : 1; }\n')
@@ -74,7 +75,7 @@ def test_temp_sizes(lib):
     t64 = (10_000_000 + 2047) // 2048
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
     assert lib.gb_temp_storage_bytes(gb.KIND_SCAN, gb.F64, 1, 10_000_000, 0) == 256 + r(t64 * 4) + 2 * r(t64 * 8)
-    for kind in range(6):
+    for kind in range(8):
         assert lib.gb_temp_storage_bytes(kind, gb.F32, 1, 12345, 17) > 0
     assert lib.gb_temp_storage_bytes(99, gb.F32, 1, 10, 10) == 0
     assert lib.gb_temp_storage_bytes(gb.KIND_SCAN, 17, 1, 10, 10) == 0
@@ -102,6 +103,24 @@ def test_argument_checks_before_cuda(lib):
     assert lib.gb_pack_by_counts(p, 10, None, None, 10, p, None, 0, None) == gb.ERR_INVALID
     assert lib.gb_pack_by_counts(p, 10, None, p, 10, None, None, 0, None) == gb.ERR_INVALID
     assert lib.gb_scan_reduce_then_scan(gb.F32, gb.MAX, 0, p, p, 10, None, None, 0, None) == gb.ERR_NO_IDENTITY
+    assert lib.gb_scan_then_fan(gb.F32, gb.MIN, 0, p, p, 10, None, None, 0, None) == gb.ERR_NO_IDENTITY
+    assert lib.gb_scan_then_fan(gb.F32, 9, 1, p, p, 10, None, None, 0, None) == gb.ERR_INVALID
+    # partition: predicates, the bit split on integers only, bit index range, sizes
+    assert lib.gb_partition(gb.F32, p, 1 << 31, gb.LT, ctypes.byref(t), p, None, p, None, 0, None) == gb.ERR_RANGE
+    assert lib.gb_partition(gb.F32, p, 10, 7, ctypes.byref(t), p, None, p, None, 0, None) == gb.ERR_INVALID
+    assert lib.gb_partition(gb.F32, p, 10, gb.BIT_CLEAR, ctypes.byref(t), p, None, p, None, 0, None) == \
+        gb.ERR_UNSUPPORTED
+    b32 = ctypes.c_int32(32)
+    assert lib.gb_partition(gb.I32, p, 10, gb.BIT_CLEAR, ctypes.byref(b32), p, None, p, None, 0, None) == \
+        gb.ERR_INVALID
+    assert lib.gb_partition(gb.F32, p, 10, gb.LT, ctypes.byref(t), None, None, p, None, 0, None) == gb.ERR_INVALID
+    assert lib.gb_partition(gb.F32, p, 10, gb.LT, ctypes.byref(t), p, None, None, None, 0, None) == gb.ERR_INVALID
+    assert lib.gb_partition(gb.F32, ctypes.c_void_p(258), 10, gb.LT, ctypes.byref(t), p, None, p, None, 0, None) == \
+        gb.ERR_INVALID  # elements must be naturally aligned
+    # segmented: identity rules as for the exclusive scans, flags required
+    assert lib.gb_scan_segmented(gb.F32, gb.MAX, 0, p, p, p, 10, None, None, 0, None) == gb.ERR_NO_IDENTITY
+    assert lib.gb_scan_segmented(gb.F32, gb.ADD, 1, p, None, p, 10, None, None, 0, None) == gb.ERR_INVALID
+    assert lib.gb_scan_segmented(gb.F32, gb.ADD, 1, p, p, p, 0, None, None, 0, None) == gb.OK
 
 
 def test_valid_call_without_gpu_fails_loudly(lib):
