@@ -311,8 +311,8 @@ template <class T> size_t compact_temp_bytes(long long n) {
   return rows > seg ? rows : seg;
 }
 
-template <class T, int PRED> cudaError_t launch_compact_seg_p(const CompactJob& job, const LaunchCtx& ctx) {
-  using G = SegGeom<T>;
+template <class T, int PRED, class G = SegGeom<T>>
+cudaError_t launch_compact_seg_p(const CompactJob& job, const LaunchCtx& ctx) {
   const SegPlan p = seg_plan<G>(1, job.n, ctx.num_sms);
   if (p.ctas == 0) return cudaSuccess;
   CompactSegArgs<T> a;
