@@ -9,19 +9,25 @@
 // the scan then runs well below the copy bandwidth even though, without the wait,
 // the same tiles move at copy speed.  The 129 MB L2 can hold that much.
 //
-// So each persistent CTA (one per SM) runs three decoupled roles over "runs" of
+// So each persistent CTA (one per SM) runs four decoupled roles over "runs" of
 // RUN consecutive tiles, claimed in order from an atomic counter (The CUDA
 // Handbook, 13.3.4: claimed order gives forward progress):
-//   L  (warp 0)   claims runs, streams their tiles from HBM into shared memory by
-//                 bulk copies (L2 evict-last hint), reduces each tile as it lands,
-//                 frees the buffer at once, and publishes the run's aggregate (A,
-//                 or P for run 0) as soon as its last tile is reduced;
-//   B  (warp 1)   takes the CTA's runs in order and computes each run's exclusive
+//   I  (one lane of warp 0)  claims runs (one claim ahead, while the CTA's queue of
+//                 QD runs has room) and streams their tiles from HBM into NL
+//                 shared-memory buffers by bulk copies (L2 evict-last hint);
+//   R  (NR warps) reduce each tile as it lands and free its buffer at once; the
+//                 reducer of a run's last tile publishes the run's aggregate (A, or
+//                 P for run 0);
+//   B  (one warp) takes the CTA's runs in order and computes each run's exclusive
 //                 prefix with the warp-cooperative decoupled look-back over run
-//                 status words, then publishes P;
-//   S  (warps 2+) re-reads each run with a known prefix tile by tile from L2 (bulk
-//                 copies, evict-first), scans it in shared memory (the same two
-//                 passes as the row kernel), and bulk-stores it (evict-first).
+//                 status words (a window of 32 x K runs per round trip), then
+//                 publishes P;
+//   S  (NG groups of NSW warps) each own whole runs of the queue: a group re-loads a
+//                 run's tiles from L2 (bulk copies, evict-first, a ring of NS
+//                 buffers) as soon as its aggregate is out, so the copies overlap
+//                 the look-back, then scans them in registers from the run's prefix
+//                 (the row kernel's two passes) and stores them as 16-byte vectors
+//                 (evict-first).
 // HBM traffic stays one read and one write per element; the second read is served
 // by L2.  I and R never wait on other CTAs, so every claimed run publishes its
 // aggregate within one load latency, and B's look-backs always end.  I claims a
