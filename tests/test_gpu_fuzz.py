@@ -7,9 +7,10 @@ reduce-then-scan kernels; the segment and tile compaction kernels) is crossed at
 random as well as at the boundaries the other test files pin.  Sizes are drawn around
 those boundaries: chunk (512 elements), tile (4096) and run (3 tiles) sizes, the size
 at which every warp of every CTA has a chunk (2,490,368), and log-uniform in between.
-The bars are the usual ones (tests/parity.py): bit-exact for integers, max/min,
-indices and partitions; the stated tolerance for float add; the product bound for
-float multiply (whose factors here are +-2^k, so exact).
+Packing by counts and the host-array scan are swept the same way.  The bars are the
+usual ones (tests/parity.py): bit-exact for integers, max/min, indices, partitions
+and records; the stated tolerance for float add; the product bound for float
+multiply (whose factors here are +-2^k, so exact).
 """
 import numpy as np
 import pytest
@@ -233,4 +234,42 @@ def test_fuzz_segmented(case):
         i = int(np.flatnonzero(~ok)[0])
         raise AssertionError("%s: %d mismatches, first at %d: got %r want %r" % (
             what, int((~ok).sum()), i, got[i], want[i]))
+    assert gb.device_error() == gb.OK, what
+
+
+@pytest.mark.parametrize("case", range(80))
+def test_fuzz_pack(case):
+    r = np.random.default_rng(13_000 + case)
+    n = draw_n(r, 1_000_000)
+    lam = float(r.choice([0.0, 0.05, 1.0, 4.0, 20.0]))
+    k = workloads.poisson_counts(n, lam, 13_000 + case)
+    total = int(k.astype(np.int64).sum())
+    cap = total + int(r.choice([0, 1, 1000]))
+    with_offsets = bool(r.random() < 0.8)
+    what = "case %d: n=%d lambda=%g cap=%d offsets=%s" % (case, n, lam, cap, with_offsets)
+    offs, recs, tot = gb.pack_by_counts(dev(k), cap, offsets=with_offsets)
+    w_offs, w_recs, w_total = oracle.pack_by_counts(k, capacity=cap)
+    assert int(tot.item()) == w_total, what
+    if with_offsets:
+        assert np.array_equal(offs.cpu().numpy()[:n].astype(np.int64), w_offs), what + ": offsets"
+    assert np.array_equal(recs.cpu().numpy()[:total], w_recs[:total]), what + ": records"
+    assert gb.device_error() == gb.OK, what
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_fuzz_host_scan(case):
+    r = np.random.default_rng(14_000 + case)
+    dt = str(r.choice(["i32", "i64", "f32", "f64"]))
+    op = str(r.choice(["add", "max", "min"]))
+    n = draw_n(r)
+    chunk = int(r.choice([0, 4096, 65_536, 1 << 20] + ([16] if n < 5000 else [])))
+    pinned = bool(r.random() < 0.7)
+    x = scan_values(dt, op, n, 14_000 + case)
+    xh = torch.from_numpy(x)
+    if pinned:
+        xh = xh.pin_memory()
+    what = "case %d: %s %s n=%d chunk=%d pinned=%s" % (case, dt, op, n, chunk, pinned)
+    out = gb.scan_inclusive_host(xh, op, chunk_elems=chunk)
+    torch.cuda.current_stream().synchronize()
+    assert_scan_matches(out.numpy(), as3(x, 1, n, 1), op, True, what=what)
     assert gb.device_error() == gb.OK, what
