@@ -57,6 +57,61 @@ template <int PRED, class T> __device__ __forceinline__ bool select_pred(T x, T 
   }
 }
 
+// Phase 1 of the selection segment kernels (compaction, partition): how many
+// elements of the warp's chunks [c0, c1) satisfy PRED.  Coalesced 16-byte vectors,
+// U per lane in flight, loaded with the L2 evict-last hint so that phase 3 finds
+// them; the ragged end element by element.  Elements before d (a partition's
+// unaligned head, read from the aligned base below the input) do not count; they
+// can only sit in the base's first vector.  Returns this lane's share.
+template <class T, int PRED, class G>
+__device__ __forceinline__ unsigned count_selected(const T* in, long long n, long long c0, long long c1, T thr,
+                                                   long long d, int lane) {
+  constexpr int VEC = G::VEC, CH = G::CH, U = 8;
+  const unsigned long long keep = l2_policy_evict_last();
+  const long long e1 = c1 * CH < n ? c1 * CH : n;
+  const long long v1 = e1 / VEC;
+  const uint4* p = reinterpret_cast<const uint4*>(in);
+  long long v = c0 * CH / VEC + lane;
+  unsigned cnt = 0;
+  if (d > 0 && v < 32 && v < v1) {  // the base's first vector may hold masked elements
+    Vec<T> x;
+    const uint4 u = ld_hint(p + v, keep);
+    memcpy(x.v, &u, 16);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) cnt += (v * VEC + e >= d && select_pred<PRED>(x.v[e], thr)) ? 1u : 0u;
+    v += 32;
+  }
+  for (; v + 32 * (U - 1) < v1; v += 32 * U) {  // U loads in flight
+    uint4 u[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      Vec<T> x;
+      memcpy(x.v, &u[k], 16);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], thr) ? 1u : 0u;
+    }
+  }
+  if (v < v1) {  // the rest in one guarded round
+    uint4 u[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (v + 32 * k < v1) {
+        Vec<T> x;
+        memcpy(x.v, &u[k], 16);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], thr) ? 1u : 0u;
+      }
+  }
+  if (lane == 0)
+    for (long long i = v1 * VEC; i < e1; ++i) cnt += (i >= d && select_pred<PRED>(in[i], thr)) ? 1u : 0u;
+  return cnt;
+}
+
 template <class T>
 __global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_kernel(CompactArgs<T> a, PackedStatus<unsigned> st) {
   pdl_entry();
@@ -195,45 +250,8 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
   long long c0, c1;
   const int nact = seg_chunks(a, seg, warp, NW, c0, c1);
 
-  // Phase 1: selected elements in the warp's part (coalesced vectors, U per lane in
-  // flight, L2 evict-last so that phase 3 finds them).
-  unsigned cnt = 0;
-  {
-    constexpr int U = 8;
-    const unsigned long long keep = l2_policy_evict_last();
-    const long long e1 = c1 * CH < a.n ? c1 * CH : a.n;
-    const long long v1 = e1 / VEC;
-    const uint4* p = reinterpret_cast<const uint4*>(a.in);
-    long long v = c0 * CH / VEC + lane;
-    for (; v + 32 * (U - 1) < v1; v += 32 * U) {  // U loads in flight
-      uint4 u[U];
-#pragma unroll
-      for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
-#pragma unroll
-      for (int k = 0; k < U; ++k) {
-        Vec<T> x;
-        memcpy(x.v, &u[k], 16);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], a.thr) ? 1u : 0u;
-      }
-    }
-    if (v < v1) {  // the rest in one guarded round
-      uint4 u[U];
-#pragma unroll
-      for (int k = 0; k < U; ++k)
-        if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
-#pragma unroll
-      for (int k = 0; k < U; ++k)
-        if (v + 32 * k < v1) {
-          Vec<T> x;
-          memcpy(x.v, &u[k], 16);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], a.thr) ? 1u : 0u;
-        }
-    }
-    if (lane == 0)
-      for (long long i = v1 * VEC; i < e1; ++i) cnt += select_pred<PRED>(a.in[i], a.thr) ? 1u : 0u;
-  }
+  // Phase 1: selected elements in the warp's part.
+  unsigned cnt = count_selected<T, PRED, G>(a.in, a.n, c0, c1, a.thr, 0, lane);
   cnt = __reduce_add_sync(0xffffffffu, cnt);
   if (lane == 0) s_warp[warp] = cnt;
   __syncthreads();

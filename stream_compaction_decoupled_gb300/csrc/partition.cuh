@@ -50,51 +50,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) partition_seg_kernel(Partition
   const long long d = a.d;
 
   // Phase 1: selected elements of the warp's part.
-  unsigned cnt = 0;
-  {
-    constexpr int U = 8;
-    const unsigned long long keep = l2_policy_evict_last();
-    const long long e1 = c1 * CH < a.n ? c1 * CH : a.n;
-    const long long v1 = e1 / VEC;
-    const uint4* p = reinterpret_cast<const uint4*>(a.in);
-    long long v = c0 * CH / VEC + lane;
-    if (v < 32 && v < v1) {  // the first vector of the base may hold masked elements
-      Vec<T> x;
-      const uint4 u = ld_hint(p + v, keep);
-      memcpy(x.v, &u, 16);
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) cnt += (v * VEC + e >= d && select_pred<PRED>(x.v[e], a.thr)) ? 1u : 0u;
-      v += 32;
-    }
-    for (; v + 32 * (U - 1) < v1; v += 32 * U) {  // U loads in flight
-      uint4 u[U];
-#pragma unroll
-      for (int k = 0; k < U; ++k) u[k] = ld_hint(p + v + 32 * k, keep);
-#pragma unroll
-      for (int k = 0; k < U; ++k) {
-        Vec<T> x;
-        memcpy(x.v, &u[k], 16);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], a.thr) ? 1u : 0u;
-      }
-    }
-    if (v < v1) {  // the rest in one guarded round
-      uint4 u[U];
-#pragma unroll
-      for (int k = 0; k < U; ++k)
-        if (v + 32 * k < v1) u[k] = ld_hint(p + v + 32 * k, keep);
-#pragma unroll
-      for (int k = 0; k < U; ++k)
-        if (v + 32 * k < v1) {
-          Vec<T> x;
-          memcpy(x.v, &u[k], 16);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) cnt += select_pred<PRED>(x.v[e], a.thr) ? 1u : 0u;
-        }
-    }
-    if (lane == 0)
-      for (long long i = v1 * VEC; i < e1; ++i) cnt += (i >= d && select_pred<PRED>(a.in[i], a.thr)) ? 1u : 0u;
-  }
+  unsigned cnt = count_selected<T, PRED, G>(a.in, a.n, c0, c1, a.thr, d, lane);
   cnt = __reduce_add_sync(0xffffffffu, cnt);
   if (lane == 0) s_warp[warp] = cnt;
   __syncthreads();
