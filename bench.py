@@ -63,6 +63,7 @@ KERNEL_SOURCES = {
     "scan_rows_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh"),
     "scan_rows_chunk_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh"),
     "scan_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh"),
+    "scan_seg_chunk_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh"),
     "compact_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "compact.cuh"),
     "compact_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_rows.cuh", "compact.cuh"),
     "partition_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "compact.cuh", "partition.cuh"),
