@@ -8,7 +8,9 @@ The arithmetic lives in ``oracle.c`` (plain C, one left-to-right loop per scanne
 line, fp64 accumulation for floating point); this module only builds it, loads it
 with ctypes and marshals numpy arrays.  Definitions followed are those of
 B. Merry, "Prefix sums on GPUs" (slides "Exclusive Prefix Sum", "Inclusive Prefix
-Sum", "Output Format", "Solution", "Other Applications": compaction, partitioning).
+Sum", "Output Format", "Solution", "Other Applications": compaction, partitioning),
+and for the one operator that is not commutative (composition of affine maps) the
+caveat on commutativity in The CUDA Handbook, 13.3.4.
 """
 from __future__ import annotations
 
@@ -55,6 +57,8 @@ def _load():
         lib.oracle_scan_segmented.restype = i
         lib.oracle_partition.argtypes = [i, vp, i64, i, vp, vp, vp]
         lib.oracle_partition.restype = i64
+        lib.oracle_scan_affine.argtypes = [i, i, vp, vp, i64, vp]
+        lib.oracle_scan_affine.restype = i
         lib.oracle_pack_by_counts.argtypes = [vp, i64, vp, vp, i64]
         lib.oracle_pack_by_counts.restype = i64
         _lib = lib
@@ -155,6 +159,24 @@ def scan_segmented(x: np.ndarray, flags: np.ndarray, op: str = "add", inclusive:
     if rc != 0:
         raise ValueError("oracle_scan_segmented rejected its arguments (%d)" % rc)
     return out[:x.size].copy()
+
+
+def scan_affine(x: np.ndarray, inclusive: bool = True, init=None) -> np.ndarray:
+    """Scan of affine maps y -> a*y + b under composition in index order (the earlier
+    map applied first).  x holds n pairs (a_i, b_i) as 2n consecutive integers (any
+    shape whose size is even); the result has x's shape and type.  init (exclusive
+    only) is a pair (a, b); None means the identity map (1, 0)."""
+    x = np.ascontiguousarray(x)
+    if x.size % 2:
+        raise ValueError("affine maps are pairs (a, b)")
+    dt = dtype_name(x)
+    out = np.empty(max(x.size, 2), dtype=x.dtype)
+    ia = None if init is None else np.ascontiguousarray(np.asarray(init).astype(x.dtype).reshape(2))
+    rc = _load().oracle_scan_affine(_DTYPES[dt], 1 if inclusive else 0, x.ctypes.data, out.ctypes.data,
+                                    x.size // 2, None if ia is None else ia.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_scan_affine rejected its arguments (%d)" % rc)
+    return out[:x.size].reshape(x.shape).copy()
 
 
 def partition(x: np.ndarray, pred: str, threshold):

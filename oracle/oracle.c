@@ -354,6 +354,89 @@ int oracle_scan_segmented(int dtype, int op, int inclusive, const void *in,
     return OR_OK;
 }
 
+/* ---- composition of affine maps ----------------------------------------------- */
+
+/*
+ * An associative operator that is not commutative, on which the order in which a
+ * scan combines its terms shows (The CUDA Handbook, 13.3.4: the packed single-pass
+ * descriptor assumes a commutative operator; combining in index order does not).
+ * Element i is the affine map f_i(y) = a_i * y + b_i of one integer type, stored as
+ * the pair (a_i, b_i) in two consecutive values.  The operator composes two maps in
+ * index order, the earlier one applied first:
+ *     (a1, b1) (+) (a2, b2) = (a1 * a2,  a2 * b1 + b2),   i.e. y -> f2(f1(y)).
+ * Its neutral element is the identity map (1, 0).  Inclusive s_i = f_0 (+) ... (+)
+ * f_i, whose b is the value y_i of the first-order linear recurrence
+ * y_i = a_i * y_{i-1} + b_i started from y_{-1} = 0; exclusive e_i = init (+) f_0
+ * (+) ... (+) f_{i-1} (init NULL: the identity).  32- and 64-bit integers wrap
+ * modulo 2^32 / 2^64 (the low bits of the exact results), so signed and unsigned
+ * types give the same bits.  One left-to-right loop, as for the other scans.
+ * Returns OR_OK or OR_BAD_ARGUMENT (a float type, or n < 0).
+ */
+int oracle_scan_affine(int dtype, int inclusive, const void *in, void *out, int64_t n,
+                       const void *init)
+{
+    if (n < 0) return OR_BAD_ARGUMENT;
+    if (dtype == OR_I32 || dtype == OR_U32) {
+        const uint32_t *x = in;
+        uint32_t *y = out;
+        uint32_t a = 1u, b = 0u;
+        if (!inclusive && init) {
+            a = ((const uint32_t *)init)[0];
+            b = ((const uint32_t *)init)[1];
+        }
+        for (int64_t i = 0; i < n; i++) {
+            uint32_t xa = x[2 * i], xb = x[2 * i + 1];
+            if (!inclusive) {
+                y[2 * i] = a;
+                y[2 * i + 1] = b;
+            }
+            if (inclusive && i == 0) {
+                a = xa;
+                b = xb;
+            } else {
+                uint32_t na = a * xa, nb = xa * b + xb;
+                a = na;
+                b = nb;
+            }
+            if (inclusive) {
+                y[2 * i] = a;
+                y[2 * i + 1] = b;
+            }
+        }
+        return OR_OK;
+    }
+    if (dtype == OR_I64 || dtype == OR_U64) {
+        const uint64_t *x = in;
+        uint64_t *y = out;
+        uint64_t a = 1u, b = 0u;
+        if (!inclusive && init) {
+            a = ((const uint64_t *)init)[0];
+            b = ((const uint64_t *)init)[1];
+        }
+        for (int64_t i = 0; i < n; i++) {
+            uint64_t xa = x[2 * i], xb = x[2 * i + 1];
+            if (!inclusive) {
+                y[2 * i] = a;
+                y[2 * i + 1] = b;
+            }
+            if (inclusive && i == 0) {
+                a = xa;
+                b = xb;
+            } else {
+                uint64_t na = a * xa, nb = xa * b + xb;
+                a = na;
+                b = nb;
+            }
+            if (inclusive) {
+                y[2 * i] = a;
+                y[2 * i + 1] = b;
+            }
+        }
+        return OR_OK;
+    }
+    return OR_BAD_ARGUMENT;
+}
+
 /* ---- partition ----------------------------------------------------------- */
 
 /* Is bit b of the element's bit pattern clear?  (Integer types.) */

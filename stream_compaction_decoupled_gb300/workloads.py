@@ -43,6 +43,13 @@ def small_ints(n: int, seed: int, lo: int = 0, hi: int = 100, dtype=np.int32) ->
     return rng(seed).integers(lo, hi, n, dtype=dtype)
 
 
+def full_range_uints(n: int, seed: int, dtype=np.uint32) -> np.ndarray:
+    """n unsigned integers uniform over the whole range of the type: about half of
+    them have the top bit set, where signed and unsigned comparisons disagree."""
+    bits = 8 * np.dtype(dtype).itemsize
+    return rng(seed).integers(0, 2 ** bits, n, dtype=np.dtype(dtype).type)
+
+
 def lognormal(n: int, dtype, seed: int, sigma: float) -> np.ndarray:
     """n factors exp(sigma * N(0, 1)): products of many stay within the type's range."""
     return np.exp(sigma * rng(seed).standard_normal(n)).astype(dtype)

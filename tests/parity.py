@@ -4,7 +4,9 @@ Bars:
   - integers, max/min, compaction indices, packing: bit-exact (max/min on floats:
     exact value equality, since they never round);
   - float add: |gpu - oracle_fp64| <= 1e-5 * (prefix sum of |x|) + 1e-6, element
-    by element and lane by lane, the prefix sum of |x| taken along the scanned axis;
+    by element and lane by lane, the prefix sum of |x| taken along the scanned axis
+    over the terms the output combines (for an exclusive scan: the elements before
+    it and the initial value);
   - float multiply: |gpu - oracle_fp64| <= gamma_k * |oracle_fp64| with k the number
     of factors at that position (plus init) and gamma_k = k u / (1 - k u), u the unit
     roundoff of the element type: the rounding bound of a product of k floats in any
@@ -52,14 +54,15 @@ def assert_scan_matches(got: np.ndarray, x3: np.ndarray, op: str, inclusive: boo
             raise AssertionError("%s: %d mismatches, first at %s: got %s want %s" % (
                 what, int((~ok).sum()), bad[0].tolist(), got[tuple(bad[0])], want[tuple(bad[0])]))
         return
-    bound = REL * abs_prefix(x3) + ABS
+    mag = abs_prefix(x3)
     if not inclusive:
-        # the exclusive value at i covers elements < i (plus init)
-        shifted = np.zeros_like(bound)
-        shifted[:, 1:, :] = bound[:, :-1, :]
-        bound = shifted + ABS
+        # the exclusive value at i covers the elements before i, plus init
+        shifted = np.zeros_like(mag)
+        shifted[:, 1:, :] = mag[:, :-1, :]
+        mag = shifted
         if init is not None:
-            bound = bound + REL * np.abs(np.asarray(init, dtype=np.float64)).reshape(1, 1, -1)
+            mag = mag + np.abs(np.asarray(init, dtype=np.float64)).reshape(1, 1, -1)
+    bound = REL * mag + ABS
     err = np.abs(got.astype(np.float64) - want)
     ok = err <= bound
     if not ok.all():

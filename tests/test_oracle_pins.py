@@ -121,6 +121,48 @@ def pin_wraparound(scan3, golden=None):
     assert [int(v) for v in one_d(scan3, xu)] == wantu
 
 
+def pin_wraparound_64(scan3, golden=None):
+    """64-bit add keeps the low 64 bits of the exact sum (Python integers)."""
+    x = np.array([2**63 - 1, 1, 2**63 - 1, -2**63, -5, 7, 2**62, 2**62], dtype=np.int64)
+    acc, want = 0, []
+    for v in x:
+        acc = _wrap(acc + int(v), 64)
+        want.append(acc)
+    assert [int(v) for v in one_d(scan3, x)] == want
+    r = np.random.default_rng(404)
+    xu = r.integers(0, 2**64, 700, dtype=np.uint64)
+    acc, wantu = 0, []
+    for v in xu:
+        acc = (acc + int(v)) % 2**64
+        wantu.append(acc)
+    assert [int(v) for v in one_d(scan3, xu)] == wantu
+    e = one_d(scan3, xu, inclusive=False, init=xu[3])
+    assert [int(v) for v in e] == [(int(xu[3]) + (w - int(v))) % 2**64 for w, v in zip(wantu, xu)]
+
+
+def pin_unsigned_max_min(scan3, golden=None):
+    """Unsigned max and min order values as unsigned integers: a value with the top
+    bit set is larger than any without it.  Full-range values (about half with the
+    top bit set) and a head whose signed and unsigned orders differ, inclusive and
+    exclusive, against Python integers."""
+    r = np.random.default_rng(303)
+    for dt, bits in ((np.uint32, 32), (np.uint64, 64)):
+        x = r.integers(0, 2**bits, 600, dtype=dt)
+        x[:3] = np.array([2**bits - 1, 1, 2**(bits - 1)], dtype=dt)
+        xs = [int(v) for v in x]
+        for op, f in (("max", max), ("min", min)):
+            acc, want = None, []
+            for v in xs:
+                acc = v if acc is None else f(acc, v)
+                want.append(acc)
+            assert [int(v) for v in one_d(scan3, x, op)] == want, (dt, op)
+            acc, want = xs[5], []
+            for v in xs:
+                want.append(acc)
+                acc = f(acc, v)
+            assert [int(v) for v in one_d(scan3, x, op, False, init=x[5])] == want, (dt, op, "excl")
+
+
 def _brute(x, op, inclusive, init):
     """Every prefix recomputed from scratch: O(n^2)."""
     n = len(x)
@@ -220,8 +262,8 @@ def pin_mul_bruteforce(scan3, golden=None):
 
 PINS = [pin_golden_definitions, pin_golden_kogge_stone, pin_golden_kary, pin_all_ones,
         pin_last_is_reduction, pin_max_min_monotone, pin_exclusive_relations,
-        pin_wraparound, pin_bruteforce, pin_axes_and_lanes, pin_mul_closed_forms,
-        pin_mul_bruteforce]
+        pin_wraparound, pin_wraparound_64, pin_unsigned_max_min, pin_bruteforce, pin_axes_and_lanes,
+        pin_mul_closed_forms, pin_mul_bruteforce]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -266,6 +308,11 @@ def _numpy_scan3(mistake):
             use = {"max": "min", "min": "max"}.get(op, op)
         if mistake == "mul_is_add":
             use = {"mul": "add"}.get(op, op)
+        signed_view = None
+        if mistake == "signed_compare" and x.dtype.kind == "u" and use in ("max", "min"):
+            signed_view = np.dtype("i%d" % x.dtype.itemsize)   # compares as if signed
+            a = a.view(signed_view)
+            acc_t = signed_view
         if mistake == "drop_first_term":
             a = a.copy()
             idx = [slice(None)] * 3
@@ -287,6 +334,9 @@ def _numpy_scan3(mistake):
             s = np.minimum.accumulate(a, axis=axis)
         if mistake == "reversed":
             s = np.flip(s, axis=axis)
+        if signed_view is not None:
+            s = s.view(x.dtype)
+            acc_t = x.dtype
         if mistake == "off_by_one":
             inclusive = not inclusive
         if inclusive:
@@ -310,7 +360,8 @@ def _numpy_scan3(mistake):
 
 
 MISTAKES = ["drop_first_term", "wrong_sign", "off_by_one", "reversed", "transposed_axis",
-            "max_is_min", "init_ignored", "fp32_accumulate", "mul_is_add", "mul_identity_zero"]
+            "max_is_min", "init_ignored", "fp32_accumulate", "mul_is_add", "mul_identity_zero",
+            "signed_compare"]
 
 
 def test_reference_numpy_scan_passes(golden):
@@ -487,3 +538,167 @@ def test_segmented_closed_forms_and_rows():
     assert np.array_equal(oracle.scan_segmented(x, fl).reshape(64, 64), np.cumsum(rows, axis=1, dtype=np.int32))
     with pytest.raises(oracle.NoIdentity):
         oracle.scan_segmented(x, fl, "max", inclusive=False)
+
+
+# -------------------------------------------- composition of affine maps --
+# Element i is the map y -> a_i*y + b_i; the operator applies the earlier map first:
+# (a1, b1) (+) (a2, b2) = (a1*a2, a2*b1 + b2).  Pins in Python integers, wrapped to
+# the type's width: the recurrence y_i = a_i*y_{i-1} + b_i, maps applied one by one
+# to a start value, the closed form for equal maps, a worked pair whose two orders
+# differ, and O(n^2) brute force.
+
+def oracle_affine(x, inclusive=True, init=None):
+    return oracle.scan_affine(x, inclusive, init)
+
+
+def _pairs(x):
+    return [(int(x[2 * i]), int(x[2 * i + 1])) for i in range(x.size // 2)]
+
+
+def _out_pairs(y, bits):
+    return [(int(a) % 2**bits, int(b) % 2**bits) for a, b in _pairs(np.asarray(y))]
+
+
+def apin_worked_pair(scan_affine):
+    """y -> 2y + 3 then y -> 5y + 1 is y -> 10y + 16; the other order is y -> 10y + 5."""
+    x = np.array([2, 3, 5, 1], dtype=np.int32)
+    assert _out_pairs(scan_affine(x), 32) == [(2, 3), (10, 16)]
+    x = np.array([5, 1, 2, 3], dtype=np.int32)
+    assert _out_pairs(scan_affine(x), 32) == [(5, 1), (10, 5)]
+    assert _out_pairs(scan_affine(np.array([5, 1, 2, 3], dtype=np.int64), False), 64) == [(1, 0), (5, 1)]
+
+
+def apin_recurrence(scan_affine):
+    """s_i = (a_0 ... a_i, y_i) with y_i = a_i y_{i-1} + b_i and y_{-1} = 0."""
+    r = np.random.default_rng(501)
+    for dt, bits in ((np.int32, 32), (np.uint32, 32), (np.int64, 64), (np.uint64, 64)):
+        x = r.integers(0, 2**bits, 2 * 700, dtype=np.uint64).astype(dt) if bits == 64 else \
+            r.integers(0, 2**bits, 2 * 700, dtype=np.uint64).astype(np.uint32).astype(dt)
+        prod, y, want = 1, 0, []
+        for a, b in _pairs(x):
+            prod = prod * a % 2**bits
+            y = (a * y + b) % 2**bits
+            want.append((prod, y))
+        assert _out_pairs(scan_affine(x), bits) == want, dt
+
+
+def apin_apply_to_start(scan_affine):
+    """The scanned map s_i sends any start value y0 where the maps f_0 .. f_i,
+    applied one after the other, send it."""
+    r = np.random.default_rng(502)
+    x = r.integers(-50, 50, 2 * 300).astype(np.int64)
+    got = _out_pairs(scan_affine(x), 64)
+    for y0 in (0, 1, -7, 123456789):
+        y = y0
+        for i, (a, b) in enumerate(_pairs(x)):
+            y = (a * y + b) % 2**64
+            ga, gb = got[i]
+            assert (ga * y0 + gb) % 2**64 == y, (y0, i)
+
+
+def apin_equal_maps(scan_affine):
+    """All maps equal to (a, b): s_i = (a^(i+1), b (1 + a + ... + a^i))."""
+    for a, b, dt, bits in ((3, 5, np.int32, 32), (-2, 7, np.int64, 64), (1, 9, np.uint32, 32)):
+        n = 1000
+        x = np.tile(np.array([a, b], dtype=np.int64), n).astype(dt)
+        want = [(a**(i + 1) % 2**bits, b * sum(a**k for k in range(i + 1)) % 2**bits) for i in range(n)]
+        assert _out_pairs(scan_affine(x), bits) == want, (a, b)
+
+
+def apin_exclusive(scan_affine):
+    """e_0 = init and e_i = init (+) s_{i-1}; no init: the identity map (1, 0)."""
+    r = np.random.default_rng(503)
+    x = r.integers(-1000, 1000, 2 * 500).astype(np.int32)
+    s = _out_pairs(scan_affine(x), 32)
+    e = _out_pairs(scan_affine(x, False), 32)
+    assert e == [(1, 0)] + s[:-1]
+    ia, ib = 7, -3
+    e = _out_pairs(scan_affine(x, False, (ia, ib)), 32)
+    want = [(ia % 2**32, ib % 2**32)] + [(ia * a % 2**32, (a * ib + b) % 2**32) for a, b in s[:-1]]
+    assert e == want
+
+
+def apin_bruteforce(scan_affine):
+    """Each prefix composed from scratch, as a Python function applied to 0 and 1."""
+    r = np.random.default_rng(504)
+    for n in (1, 2, 31, 33, 150):
+        x = r.integers(-9, 9, 2 * n).astype(np.int64)
+        ps = _pairs(x)
+        got = _out_pairs(scan_affine(x), 64)
+        for i in range(n):
+            def f(y, i=i):
+                for a, b in ps[: i + 1]:
+                    y = a * y + b
+                return y % 2**64
+            b0, b1 = f(0), f(1)
+            assert got[i] == ((b1 - b0) % 2**64, b0), (n, i)
+
+
+APINS = [apin_worked_pair, apin_recurrence, apin_apply_to_start, apin_equal_maps, apin_exclusive,
+         apin_bruteforce]
+
+
+@pytest.mark.parametrize("pin", APINS, ids=lambda p: p.__name__)
+def test_oracle_affine_pins(pin):
+    pin(oracle_affine)
+
+
+def test_oracle_affine_rejects_floats_and_odd_sizes():
+    with pytest.raises(ValueError):
+        oracle.scan_affine(np.ones(4, np.float32))
+    with pytest.raises(ValueError):
+        oracle.scan_affine(np.ones(3, np.int32))
+    assert oracle.scan_affine(np.zeros(0, np.int32)).size == 0
+
+
+def _python_affine(mistake):
+    """A Python stand-in for the affine scan with one plausible mistake planted."""
+    def scan_affine(x, inclusive=True, init=None):
+        x = np.asarray(x)
+        bits = 8 * x.dtype.itemsize
+        m = 2**bits
+
+        def comb(l, r_):
+            (a1, b1), (a2, b2) = l, r_
+            if mistake == "swapped_order":
+                return (a2 * a1 % m, (a1 * b2 + b1) % m)
+            if mistake == "b_unscaled":
+                return (a1 * a2 % m, (b1 + b2) % m)
+            if mistake == "scaled_by_first":
+                return (a1 * a2 % m, (a1 * b1 + b2) % m)
+            return (a1 * a2 % m, (a2 * b1 + b2) % m)
+        acc = (1, 0) if (inclusive or init is None) else (int(init[0]) % m, int(init[1]) % m)
+        if mistake == "identity_zero" and not inclusive and init is None:
+            acc = (0, 0)
+        out = []
+        for i, p in enumerate(_pairs(x)):
+            p = (p[0] % m, p[1] % m)
+            if inclusive:
+                acc = p if i == 0 else comb(acc, p)
+                out.append(acc)
+            else:
+                out.append(acc)
+                acc = comb(acc, p)
+        flat = [v for pair in out for v in pair]
+        return np.array(flat, dtype=np.uint64 if bits == 64 else np.uint32).astype(x.dtype) if flat else \
+            np.zeros(0, x.dtype)
+    return scan_affine
+
+
+AFFINE_MISTAKES = ["swapped_order", "b_unscaled", "scaled_by_first", "identity_zero"]
+
+
+def test_affine_stand_in_passes():
+    for pin in APINS:
+        pin(_python_affine("none"))
+
+
+@pytest.mark.parametrize("mistake", AFFINE_MISTAKES)
+def test_affine_pins_catch_planted_mistake(mistake):
+    failures = 0
+    for pin in APINS:
+        try:
+            pin(_python_affine(mistake))
+        except (AssertionError, ValueError, OverflowError):
+            failures += 1
+    assert failures >= 1, "no pin caught the planted mistake %r" % mistake
