@@ -370,6 +370,32 @@ def secondary_workloads(device, hbm_peak, reps=10, only=None):
 
 # ---------------------------------------------------------------- CPU oracle ---
 
+def host_cpu() -> dict:
+    """The host the oracle runs on: its logical CPU count and CPU model (lscpu's
+    "Model name", else /proc/cpuinfo's, else the machine type)."""
+    import platform
+    import subprocess
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"host_cpus": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
 def cpu_oracle_leg(x_full: np.ndarray, steps: int, budget_s: float):
     """The oracle timed on the host: `steps` inclusive scans of a leading slice of the
     headline input, its length chosen so that all steps take about budget_s."""
@@ -403,7 +429,8 @@ def reference_arm(args, rank):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 in, f64 accumulate",
             "data": "synthetic", "config": {"workload": "fp32_1e8 inclusive scan (sample, see cpu_baseline)"},
-            "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": dict({"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                  "sample": sample}, **host_cpu()),
             "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -507,6 +534,7 @@ def our_arm(args, rank, world, local_rank):
         cpu = {"value": round(2 * n_s * 4 / t / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": "fp32 inclusive scan of %d of the headline's values (fp64 accumulation), best of 3, "
                          "one host thread" % n_s}
+        cpu.update(host_cpu())  # the machine's cores and CPU model beside the one thread used
 
     if rank != 0:
         return

@@ -44,7 +44,9 @@
  *   - Return value: GB_OK or one of the GB_ERR_* codes below.  Argument errors
  *     are reported before anything is enqueued.  Errors found on the device
  *     (a look-back that waited too long, a packing capacity exceeded, a negative
- *     count) are sticky per device and are read with gb_device_error().
+ *     count) are recorded twice: in a word in the call's own scratch, read with
+ *     gb_last_device_error(temp, stream), and in a word per device that every
+ *     call shares, read (and cleared) with gb_device_error(stream).
  */
 #ifndef GBSCAN_H
 #define GBSCAN_H
@@ -70,7 +72,21 @@ enum gb_dtype { GB_I32 = 0, GB_U32 = 1, GB_I64 = 2, GB_U64 = 3, GB_F32 = 4, GB_F
  * rounding bounds of any bracketing: sums within 1e-5 of the prefix sum of |x|,
  * products within a relative (i + 1) u / (1 - (i + 1) u) at position i (u the
  * unit roundoff of the type). */
-enum gb_op { GB_ADD = 0, GB_MAX = 1, GB_MIN = 2, GB_MUL = 3 };
+enum gb_op { GB_ADD = 0, GB_MAX = 1, GB_MIN = 2, GB_MUL = 3, GB_AFFINE = 4 };
+
+/* GB_AFFINE: composition of affine maps, an operator that is associative but NOT
+ * commutative ([HB] 13.3.4 notes that its packed single-pass descriptor assumes a
+ * commutative operator; this library combines in index order throughout).  An
+ * element is the map y -> a*y + b over an integer type, stored as lanes = 2 values
+ * (a, b); the earlier map is applied first:
+ *     (a1, b1) (+) (a2, b2) = (a1*a2, a2*b1 + b2),    neutral element (1, 0).
+ * The b of inclusive output i is y_i of the recurrence y_i = a_i*y_{i-1} + b_i
+ * from y_{-1} = 0.  Arithmetic wraps modulo 2^32 / 2^64 (signed and unsigned types
+ * give the same bits).  Served by gb_scan_inclusive / gb_scan_exclusive with
+ * lanes = 2 and an integer dtype (else GB_ERR_UNSUPPORTED), `in` and `out` aligned
+ * to the element type; exclusive init is a host pointer to one map (a, b), NULL
+ * meaning (1, 0).  gb_temp_storage_bytes(GB_KIND_SCAN, dtype, 2, n, 0) covers it.
+ * The other entry points return GB_ERR_UNSUPPORTED for it. */
 
 /* Compaction and partition predicates: element x is selected when  x <op> threshold,
  * compared in the element type (a NaN fails every comparison but NE).  GB_BIT_CLEAR
@@ -191,7 +207,7 @@ int gb_scan_segmented(int dtype, int op, int inclusive, const void* in, const ui
  *   offsets       NULL, or n int32 entries that receive the start of each run
  *   out_capacity  entries available in out_records; records past it are dropped
  *   out_total     device int32: the total record count (sum of counts)
- * Device errors (gb_device_error): GB_ERR_RANGE when the total exceeds
+ * Device errors (gb_last_device_error, gb_device_error): GB_ERR_RANGE when the total exceeds
  * out_capacity or INT32_MAX; GB_ERR_INVALID when a count is negative (it is then
  * treated as 0).  temp kind: GB_KIND_PACK.
  */
@@ -290,10 +306,29 @@ size_t gb_temp_storage_bytes(int kind, int dtype, int lanes, int64_t rows, int64
 
 /*
  * Synchronise `stream`, then return and clear the sticky device-side error of the
- * current device: GB_OK, GB_ERR_TIMEOUT, GB_ERR_RANGE or GB_ERR_INVALID (the
- * first kind seen since the last read), or GB_ERR_CUDA if the sync failed.
+ * current device: GB_OK, GB_ERR_TIMEOUT, GB_ERR_RANGE or GB_ERR_INVALID (the most
+ * serious kind seen by any call on the device since the last read), or GB_ERR_CUDA
+ * if the sync failed.  Calls on independent streams all report here.
  */
 int gb_device_error(void* stream);
+
+/*
+ * The device-side status of the last call that ran kernels with this scratch
+ * ([HB] 13.3.4, Listing 13-15: the scan's scratch is the call's own; the error
+ * word sits in its header and the call clears it together with the tile-status
+ * words, so nothing from an earlier call shows): synchronises `stream` (the stream
+ * that call ran on), then returns GB_OK, GB_ERR_TIMEOUT, GB_ERR_RANGE or
+ * GB_ERR_INVALID, or GB_ERR_CUDA if the sync failed.  Unlike gb_device_error it
+ * sees only that call, so calls on other streams with their own scratch do not
+ * mix in, and it clears nothing.
+ *   temp    the `temp` the call was given (256-byte aligned), or the `work` of
+ *           gb_scan_inclusive_host (whose word gathers every chunk of the call).
+ *           A call given temp = NULL uses library scratch that is gone when it
+ *           returns: read such calls with gb_device_error.  A call that ran no
+ *           kernel (n = 0, an argument error) leaves the word as it was.
+ * Errors: GB_ERR_INVALID for a NULL or unaligned temp.
+ */
+int gb_last_device_error(void* temp, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* gb_status_string(int status);
@@ -317,7 +352,7 @@ void gb_set_profile_events(void* before, void* after);
 /*
  * Time limit, in nanoseconds of the GPU's global timer, of every wait inside the
  * kernels (a look-back waiting on a predecessor, a tile waiting for its copy).  A
- * wait that runs out records GB_ERR_TIMEOUT (see gb_device_error), publishes what
+ * wait that runs out records GB_ERR_TIMEOUT (see gb_last_device_error), publishes what
  * it has so that later tiles do not wait as well, and the kernel returns normally.
  * 0 restores the default of one second.  Process-wide.
  */

@@ -19,13 +19,13 @@ LIB_PATH = os.path.join(_HERE, "libgbscan.so")
 
 # Mirrors of the enums in include/gbscan.h.
 I32, U32, I64, U64, F32, F64 = range(6)
-ADD, MAX, MIN, MUL = range(4)
+ADD, MAX, MIN, MUL, AFFINE = range(5)
 LT, LE, GT, GE, EQ, NE, BIT_CLEAR = range(7)
 KIND_SCAN, KIND_BATCHED_AXIS1, KIND_BATCHED_AXIS0, KIND_COMPACT, KIND_PACK, KIND_REDUCE_THEN_SCAN, \
     KIND_PARTITION, KIND_SEGMENTED = range(8)
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_TEMP, ERR_NO_IDENTITY, ERR_RANGE, ERR_CUDA, ERR_TIMEOUT = range(8)
 
-OPS = {"add": ADD, "max": MAX, "min": MIN, "mul": MUL}
+OPS = {"add": ADD, "max": MAX, "min": MIN, "mul": MUL, "affine": AFFINE}
 PREDS = {"lt": LT, "le": LE, "gt": GT, "ge": GE, "eq": EQ, "ne": NE, "bit_clear": BIT_CLEAR}
 _NP_OF = {I32: np.int32, U32: np.uint32, I64: np.int64, U64: np.uint64, F32: np.float32, F64: np.float64}
 
@@ -43,6 +43,7 @@ SIGNATURES = {
     "gb_scan_segmented": (_i, [_i, _i, _i, _vp, _vp, _vp, _i64, _vp, _vp, _sz, _vp]),
     "gb_temp_storage_bytes": (_sz, [_i, _i, _i, _i64, _i64]),
     "gb_device_error": (_i, [_vp]),
+    "gb_last_device_error": (_i, [_vp, _vp]),
     "gb_status_string": (ctypes.c_char_p, [_i]),
     "gb_last_cuda_error": (_i, []),
     "gb_version": (_i, []),
@@ -110,14 +111,29 @@ def _need_cuda(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
-def _temp(x, kind, dtype, lanes, rows, cols, temp):
+def _torch_stream(x, stream):
+    """The torch stream a call runs on: the current one, or the caller's (a
+    torch.cuda.Stream, or any object with a cuda_stream handle, or a raw handle)."""
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream(x.device)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return torch.cuda.ExternalStream(handle, device=x.device)
+
+
+def _temp(x, kind, dtype, lanes, rows, cols, temp, stream=None):
     import torch
     if temp is not None:
         return ctypes.c_void_p(temp.data_ptr()), temp.numel() * temp.element_size()
     nbytes = load().gb_temp_storage_bytes(kind, dtype, lanes, rows, cols)
-    # Freed when the call returns: the caching allocator only hands the block to later
-    # allocations on the same stream, which run after this call's kernels.
-    buf = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
+    # Allocated on the stream the call runs on and freed when the call returns: the
+    # caching allocator hands the block only to later allocations on that stream,
+    # which run after this call's kernels.  (Allocated on another stream, the block
+    # could go to work on that stream while the kernels still use it.)
+    with torch.cuda.stream(_torch_stream(x, stream)):
+        buf = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
     return ctypes.c_void_p(buf.data_ptr()), nbytes
 
 
@@ -139,7 +155,7 @@ def scan_inclusive(x, op: str = "add", lanes: int = 1, out=None, temp=None, stre
     out = torch.empty_like(x) if out is None else out
     _need_cuda(x, out)
     code, n = dtype_code(x.dtype), x.numel() // lanes
-    tp, tb = _temp(x, KIND_SCAN, code, lanes, n, 0, temp)
+    tp, tb = _temp(x, KIND_SCAN, code, lanes, n, 0, temp, stream)
     _check(load().gb_scan_inclusive(code, lanes, OPS[op], ctypes.c_void_p(x.data_ptr()),
                                     ctypes.c_void_p(out.data_ptr()), n, tp, tb, _stream(x, stream)),
            "gb_scan_inclusive")
@@ -153,7 +169,7 @@ def scan_exclusive(x, op: str = "add", init=None, lanes: int = 1, out=None, temp
     _need_cuda(x, out)
     code, n = dtype_code(x.dtype), x.numel() // lanes
     keep, ip = _host_value(code, init, lanes)
-    tp, tb = _temp(x, KIND_SCAN, code, lanes, n, 0, temp)
+    tp, tb = _temp(x, KIND_SCAN, code, lanes, n, 0, temp, stream)
     _check(load().gb_scan_exclusive(code, lanes, OPS[op], ctypes.c_void_p(x.data_ptr()),
                                     ctypes.c_void_p(out.data_ptr()), n, ip, tp, tb, _stream(x, stream)),
            "gb_scan_exclusive")
@@ -171,7 +187,7 @@ def scan_batched(x, axis: int, op: str = "add", inclusive: bool = True, init=Non
     code = dtype_code(x.dtype)
     keep, ip = _host_value(code, init, lanes)
     kind = KIND_BATCHED_AXIS1 if axis == 1 else KIND_BATCHED_AXIS0
-    tp, tb = _temp(x, kind, code, lanes, rows, cols, temp)
+    tp, tb = _temp(x, kind, code, lanes, rows, cols, temp, stream)
     _check(load().gb_scan_batched(code, lanes, OPS[op], 1 if inclusive else 0, ctypes.c_void_p(x.data_ptr()),
                                   ctypes.c_void_p(out.data_ptr()), rows, cols, axis, ip, tp, tb,
                                   _stream(x, stream)), "gb_scan_batched")
@@ -188,7 +204,7 @@ def compact(x, pred: str, threshold, out_idx=None, out_count=None, temp=None, st
     _need_cuda(x, out_idx, out_count)
     code = dtype_code(x.dtype)
     keep, tptr = _host_value(code, threshold, 1)
-    tp, tb = _temp(x, KIND_COMPACT, code, 1, n, 0, temp)
+    tp, tb = _temp(x, KIND_COMPACT, code, 1, n, 0, temp, stream)
     _check(load().gb_compact(code, ctypes.c_void_p(x.data_ptr()), n, PREDS[pred], tptr,
                              ctypes.c_void_p(out_idx.data_ptr()), ctypes.c_void_p(out_count.data_ptr()),
                              tp, tb, _stream(x, stream)), "gb_compact")
@@ -210,7 +226,7 @@ def partition(x, pred: str, threshold, with_idx: bool = True, out=None, out_idx=
     _need_cuda(x, out, out_count)
     code = dtype_code(x.dtype)
     keep, tptr = _host_value(code, threshold, 1)
-    tp, tb = _temp(x, KIND_PARTITION, code, 1, n, 0, temp)
+    tp, tb = _temp(x, KIND_PARTITION, code, 1, n, 0, temp, stream)
     _check(load().gb_partition(code, ctypes.c_void_p(x.data_ptr()), n, PREDS[pred], tptr,
                                ctypes.c_void_p(out.data_ptr()),
                                ctypes.c_void_p(out_idx.data_ptr()) if out_idx is not None else None,
@@ -231,7 +247,7 @@ def pack_by_counts(counts, capacity: int, offsets: bool = True, out_records=None
     _need_cuda(counts, offs, out_records, out_total)
     if counts.dtype.itemsize != 4 or counts.dtype.is_floating_point:
         raise TypeError("counts must be int32")
-    tp, tb = _temp(counts, KIND_PACK, I32, 1, n, 0, temp)
+    tp, tb = _temp(counts, KIND_PACK, I32, 1, n, 0, temp, stream)
     _check(load().gb_pack_by_counts(ctypes.c_void_p(counts.data_ptr()), n,
                                     ctypes.c_void_p(offs.data_ptr()) if offs is not None else None,
                                     ctypes.c_void_p(out_records.data_ptr()), capacity,
@@ -275,7 +291,7 @@ def scan_reduce_then_scan(x, op: str = "add", inclusive: bool = True, init=None,
     _need_cuda(x, out)
     code, n = dtype_code(x.dtype), x.numel()
     keep, ip = _host_value(code, init, 1)
-    tp, tb = _temp(x, KIND_REDUCE_THEN_SCAN, code, 1, n, 0, temp)
+    tp, tb = _temp(x, KIND_REDUCE_THEN_SCAN, code, 1, n, 0, temp, stream)
     _check(load().gb_scan_reduce_then_scan(code, OPS[op], 1 if inclusive else 0, ctypes.c_void_p(x.data_ptr()),
                                            ctypes.c_void_p(out.data_ptr()), n, ip, tp, tb, _stream(x, stream)),
            "gb_scan_reduce_then_scan")
@@ -288,6 +304,14 @@ def device_error(stream=None) -> int:
     import torch
     s = ctypes.c_void_p(stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream)
     return load().gb_device_error(s)
+
+
+def last_device_error(temp, stream=None) -> int:
+    """Synchronise and return the device-side status of the last call that ran with
+    this scratch tensor (its `temp`, or the host scan's `work`)."""
+    import torch
+    s = _stream(temp, stream)
+    return load().gb_last_device_error(ctypes.c_void_p(temp.data_ptr()), s)
 
 
 def _event_handle(ev):
@@ -320,7 +344,7 @@ def scan_then_fan(x, op: str = "add", inclusive: bool = True, init=None, out=Non
     _need_cuda(x, out)
     code, n = dtype_code(x.dtype), x.numel()
     keep, ip = _host_value(code, init, 1)
-    tp, tb = _temp(x, KIND_REDUCE_THEN_SCAN, code, 1, n, 0, temp)
+    tp, tb = _temp(x, KIND_REDUCE_THEN_SCAN, code, 1, n, 0, temp, stream)
     _check(load().gb_scan_then_fan(code, OPS[op], 1 if inclusive else 0, ctypes.c_void_p(x.data_ptr()),
                                    ctypes.c_void_p(out.data_ptr()), n, ip, tp, tb, _stream(x, stream)),
            "gb_scan_then_fan")
@@ -340,7 +364,7 @@ def scan_segmented(x, flags, op: str = "add", inclusive: bool = True, init=None,
     _need_cuda(x, out, flags)
     code, n = dtype_code(x.dtype), x.numel()
     keep, ip = _host_value(code, init, 1)
-    tp, tb = _temp(x, KIND_SEGMENTED, code, 1, n, 0, temp)
+    tp, tb = _temp(x, KIND_SEGMENTED, code, 1, n, 0, temp, stream)
     _check(load().gb_scan_segmented(code, OPS[op], 1 if inclusive else 0, ctypes.c_void_p(x.data_ptr()),
                                     ctypes.c_void_p(flags.data_ptr()), ctypes.c_void_p(out.data_ptr()), n, ip,
                                     tp, tb, _stream(x, stream)), "gb_scan_segmented")

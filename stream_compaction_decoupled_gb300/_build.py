@@ -80,6 +80,49 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
     return LIB
 
 
+def ptxas_report(jobs: int | None = None) -> list:
+    """Compile every translation unit with -Xptxas -v into a scratch directory (the
+    library itself is left alone) and return, per kernel instantiation, what ptxas
+    reports: {"unit", "kernel", "registers", "smem", "stack", "spill_stores",
+    "spill_loads"}.  This is the compile matrix over element types, operators and
+    geometries that the library's kernels are instantiated for."""
+    import re
+    import tempfile
+    cc = nvcc()
+    pat_fn = re.compile(r"Compiling entry function '([^']+)'")
+    pat_use = re.compile(r"Used (\d+) registers(?:, used \d+ barriers)?(?:, [^,]*?stack size)?(?:, (\d+) bytes smem)?")
+    pat_spill = re.compile(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads")
+    with tempfile.TemporaryDirectory() as tmp:
+        def one(src):
+            obj = os.path.join(tmp, os.path.basename(src)[:-3] + ".o")
+            r = subprocess.run([cc] + FLAGS + ["-Xptxas", "-v", "-c", src, "-o", obj], capture_output=True, text=True)
+            if r.returncode != 0:
+                raise RuntimeError("nvcc failed on %s:\n%s%s" % (src, r.stdout, r.stderr))
+            rows, cur = [], None
+            for line in r.stderr.splitlines():
+                m = pat_fn.search(line)
+                if m:
+                    cur = {"unit": os.path.basename(src), "kernel": m.group(1), "registers": None, "smem": 0,
+                           "stack": None, "spill_stores": None, "spill_loads": None}
+                    rows.append(cur)
+                    continue
+                if cur is None:
+                    continue
+                m = pat_spill.search(line)
+                if m:
+                    cur["stack"], cur["spill_stores"], cur["spill_loads"] = (int(g) for g in m.groups())
+                    continue
+                m = pat_use.search(line)
+                if m:
+                    cur["registers"] = int(m.group(1))
+                    cur["smem"] = int(m.group(2) or 0)
+            return rows
+        srcs = _sources()
+        n = jobs or min(len(srcs), os.cpu_count() or 4)
+        with cf.ThreadPoolExecutor(max_workers=n) as ex:
+            return [row for rows in ex.map(one, srcs) for row in rows]
+
+
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))

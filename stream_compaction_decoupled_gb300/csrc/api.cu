@@ -60,6 +60,14 @@ int cuda_fail(cudaError_t e) {
   return GB_ERR_CUDA;
 }
 
+// The status code of a set of device error bits (the most serious first).
+int status_of_bits(unsigned bits) {
+  if (bits & gbs::ERRBIT_TIMEOUT) return GB_ERR_TIMEOUT;
+  if (bits & gbs::ERRBIT_RANGE) return GB_ERR_RANGE;
+  if (bits & gbs::ERRBIT_INVALID) return GB_ERR_INVALID;
+  return GB_OK;
+}
+
 // Per-device set-up (once): the address of the error word and the SM count.
 int make_ctx(void* stream, LaunchCtx& ctx) {
   int dev = 0;
@@ -78,7 +86,8 @@ int make_ctx(void* stream, LaunchCtx& ctx) {
       g_num_sms[dev] = sms;
       g_err_ptr[dev] = (unsigned*)p;
     }
-    ctx.err = g_err_ptr[dev];
+    ctx.err.dev = g_err_ptr[dev];
+    ctx.err.call = nullptr;
     ctx.num_sms = g_num_sms[dev];
   }
   ctx.stream = (cudaStream_t)stream;
@@ -99,6 +108,12 @@ struct Temp {
     if (owned && p) cudaFreeAsync(p, s);
   }
 };
+
+// The call's own error word lives in its scratch header (cleared by the call's
+// status clear), so gb_last_device_error(temp, ...) reports what this call found.
+void attach_call_err(LaunchCtx& ctx, void* temp) {
+  ctx.err.call = (unsigned*)((char*)temp + gbs::kCallErrOffset);
+}
 
 int get_temp(void* temp, size_t temp_bytes, size_t need, cudaStream_t s, Temp& t) {
   t.s = s;
@@ -126,6 +141,44 @@ size_t dtype_size(int dtype) {
 }
 
 bool valid_op(int op) { return op == GB_ADD || op == GB_MAX || op == GB_MIN || op == GB_MUL; }
+bool is_int(int dtype) { return dtype == GB_I32 || dtype == GB_U32 || dtype == GB_I64 || dtype == GB_U64; }
+
+// Scratch for a 1-D scan of affine maps (8- or 16-byte pairs of an integer type).
+size_t affine_temp(int dtype, long long n) {
+  return dtype_size(dtype) == 4 ? gbs::affine_temp_bytes<uint32_t>(n) : gbs::affine_temp_bytes<uint64_t>(n);
+}
+
+// The scan of affine maps: one row of n maps, each `lanes` = 2 integers (a, b); the
+// signed types run as the unsigned ones of their width (the same bits).
+int run_affine(int dtype, int inclusive, const void* in, void* out, long long n, const void* init, int lanes,
+               void* temp, size_t temp_bytes, void* stream) {
+  if (!dtype_size(dtype) || lanes < 1 || n < 0) return GB_ERR_INVALID;
+  if (!is_int(dtype) || lanes != 2) return GB_ERR_UNSUPPORTED;
+  if (n == 0) return GB_OK;
+  if (!in || !out) return GB_ERR_INVALID;
+  if ((uintptr_t)in % dtype_size(dtype) || (uintptr_t)out % dtype_size(dtype)) return GB_ERR_INVALID;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  Temp t;
+  rc = get_temp(temp, temp_bytes, affine_temp(dtype, n), ctx.stream, t);
+  if (rc) return rc;
+  attach_call_err(ctx, t.p);
+  gbs::ScanJob job;
+  job.op = GB_AFFINE;
+  job.inclusive = inclusive ? 1 : 0;
+  job.in = in;
+  job.out = out;
+  job.B = 1;
+  job.R = n;
+  job.C = 2;
+  job.init_host = inclusive ? nullptr : init;
+  job.init_lanes = 2;
+  job.temp = t.p;
+  const cudaError_t e = dtype_size(dtype) == 4 ? gbs::launch_affine<uint32_t>(job, ctx)
+                                               : gbs::launch_affine<uint64_t>(job, ctx);
+  return e == cudaSuccess ? GB_OK : cuda_fail(e);
+}
 bool has_identity(int op) { return op == GB_ADD || op == GB_MUL; }
 
 // Calls f.template operator()<T>() with T the C++ type of `dtype`.
@@ -191,6 +244,7 @@ int run_scan(int dtype, int op, int inclusive, const void* in, void* out, long l
   Temp t;
   rc = get_temp(temp, temp_bytes, scan_temp(dtype, B, R, C), ctx.stream, t);
   if (rc) return rc;
+  attach_call_err(ctx, t.p);
   std::vector<unsigned char> neutral;
   if (!inclusive && !init) {  // add / multiply without init: start from 0 / 1
     neutral = identity_bytes(dtype, op, lanes);
@@ -265,21 +319,26 @@ long long host_chunk_elems(int dtype, long long n, long long req) {
   return c < n ? c : n;
 }
 
+// Work area: [header: the call's error word][scan scratch][two carries][ring].  The
+// chunk scans clear only their own scratch, so the header's error word collects what
+// every chunk of the call found.
 struct HostLayout {
-  size_t scan_temp = 0, carry = 0, slot = 0, total = 0;
+  size_t header = 0, scan_temp = 0, carry = 0, slot = 0, total = 0;
 };
 HostLayout host_layout(int dtype, long long chunk) {
   HostLayout L;
+  L.header = gbs::kHeaderBytes;
   L.scan_temp = gbs::round_up(scan_temp(dtype, 1, chunk, 1), 256);
   L.carry = 256;  // two carries
   L.slot = gbs::round_up((size_t)chunk * dtype_size(dtype), 256);
-  L.total = L.scan_temp + L.carry + kRing * L.slot;
+  L.total = L.header + L.scan_temp + L.carry + kRing * L.slot;
   return L;
 }
 
 // The reduce-then-scan (stf = 0) and scan-then-fan (stf = 1) comparators.
 int run_comparator(int stf, int dtype, int op, int inclusive, const void* in, void* out, int64_t n,
                    const void* init, void* temp, size_t temp_bytes, void* stream) {
+  if (op == GB_AFFINE) return GB_ERR_UNSUPPORTED;
   if (!dtype_size(dtype) || !valid_op(op) || n < 0) return GB_ERR_INVALID;
   if (!inclusive && !init && !has_identity(op)) return GB_ERR_NO_IDENTITY;
   if (n == 0) return GB_OK;
@@ -294,6 +353,7 @@ int run_comparator(int stf, int dtype, int op, int inclusive, const void* in, vo
   Temp t;
   rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
   if (rc) return rc;
+  attach_call_err(ctx, t.p);
   const std::vector<unsigned char> neutral = identity_bytes(dtype, op, 1);
   gbs::RtsJob job;
   job.op = op;
@@ -322,6 +382,7 @@ size_t gb_host_scan_work_bytes(int dtype, int64_t n, int64_t chunk_elems) {
 
 int gb_scan_inclusive_host(int dtype, int op, const void* in_host, void* out_host, int64_t n, int64_t chunk_elems,
                            void* work, size_t work_bytes, void* stream) {
+  if (op == GB_AFFINE) return GB_ERR_UNSUPPORTED;
   if (!dtype_size(dtype) || !valid_op(op) || n < 0 || chunk_elems < 0) return GB_ERR_INVALID;
   if (n == 0) return GB_OK;
   if (!in_host || !out_host) return GB_ERR_INVALID;
@@ -338,14 +399,16 @@ int gb_scan_inclusive_host(int dtype, int op, const void* in_host, void* out_hos
   rc = get_temp(work, work_bytes, L.total, ctx.stream, t);
   if (rc) return rc;
   char* base = (char*)t.p;
-  void* scan_tmp = base;
-  char* carry = base + L.scan_temp;
+  attach_call_err(ctx, base);
+  void* scan_tmp = base + L.header;
+  char* carry = base + L.header + L.scan_temp;
   char* ring = carry + L.carry;
   const size_t es = dtype_size(dtype);
   const long long nchunks = (n + chunk - 1) / chunk;
 
   std::lock_guard<std::mutex> lk(pipe->mu);
-  cudaError_t e = cudaEventRecord(pipe->start, ctx.stream);  // after the caller's earlier work
+  cudaError_t e = cudaMemsetAsync(ctx.err.call, 0, sizeof(unsigned), ctx.stream);
+  if (e == cudaSuccess) e = cudaEventRecord(pipe->start, ctx.stream);  // after the caller's earlier work
   if (e == cudaSuccess) e = cudaStreamWaitEvent(pipe->h2d, pipe->start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(pipe->d2h, pipe->start, 0);
   for (long long i = 0; i < nchunks && e == cudaSuccess; ++i) {
@@ -392,17 +455,20 @@ int gb_scan_inclusive_host(int dtype, int op, const void* in_host, void* out_hos
 int gb_scan_inclusive(int dtype, int lanes, int op, const void* in, void* out, int64_t n, void* temp,
                       size_t temp_bytes, void* stream) {
   if (n < 0) return GB_ERR_INVALID;
+  if (op == GB_AFFINE) return run_affine(dtype, 1, in, out, n, nullptr, lanes, temp, temp_bytes, stream);
   return run_scan(dtype, op, 1, in, out, 1, n, lanes, nullptr, lanes, temp, temp_bytes, stream);
 }
 
 int gb_scan_exclusive(int dtype, int lanes, int op, const void* in, void* out, int64_t n, const void* init,
                       void* temp, size_t temp_bytes, void* stream) {
   if (n < 0) return GB_ERR_INVALID;
+  if (op == GB_AFFINE) return run_affine(dtype, 0, in, out, n, init, lanes, temp, temp_bytes, stream);
   return run_scan(dtype, op, 0, in, out, 1, n, lanes, init, lanes, temp, temp_bytes, stream);
 }
 
 int gb_scan_batched(int dtype, int lanes, int op, int inclusive, const void* in, void* out, int64_t rows,
                     int64_t cols, int axis, const void* init, void* temp, size_t temp_bytes, void* stream) {
+  if (op == GB_AFFINE) return GB_ERR_UNSUPPORTED;
   if (rows < 0 || cols < 0 || lanes < 1 || lanes > kMaxLanes) return GB_ERR_INVALID;
   if (axis == 1) return run_scan(dtype, op, inclusive, in, out, rows, cols, lanes, init, lanes, temp, temp_bytes, stream);
   if (axis == 0) {
@@ -433,6 +499,7 @@ int gb_compact(int dtype, const void* in, int64_t n, int pred, const void* thres
   Temp t;
   rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
   if (rc) return rc;
+  attach_call_err(ctx, t.p);
   gbs::CompactJob job;
   job.in = in;
   job.n = n;
@@ -477,6 +544,7 @@ int gb_partition(int dtype, const void* in, int64_t n, int pred, const void* thr
   Temp t;
   rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
   if (rc) return rc;
+  attach_call_err(ctx, t.p);
   gbs::PartitionJob job;
   job.in = in;
   job.n = n;
@@ -495,6 +563,7 @@ int gb_partition(int dtype, const void* in, int64_t n, int pred, const void* thr
 
 int gb_scan_segmented(int dtype, int op, int inclusive, const void* in, const uint8_t* flags, void* out,
                       int64_t n, const void* init, void* temp, size_t temp_bytes, void* stream) {
+  if (op == GB_AFFINE) return GB_ERR_UNSUPPORTED;
   if (!dtype_size(dtype) || !valid_op(op) || n < 0) return GB_ERR_INVALID;
   if (!inclusive && !init && !has_identity(op)) return GB_ERR_NO_IDENTITY;
   if (n == 0) return GB_OK;
@@ -509,6 +578,7 @@ int gb_scan_segmented(int dtype, int op, int inclusive, const void* in, const ui
   Temp t;
   rc = get_temp(temp, temp_bytes, need, ctx.stream, t);
   if (rc) return rc;
+  attach_call_err(ctx, t.p);
   const std::vector<unsigned char> neutral = identity_bytes(dtype, op, 1);
   gbs::SegmentedJob job;
   job.op = op;
@@ -542,6 +612,7 @@ int gb_pack_by_counts(const int32_t* counts, int64_t n, int32_t* offsets, int32_
   Temp t;
   rc = get_temp(temp, temp_bytes, gbs::pack_temp_bytes(n), ctx.stream, t);
   if (rc) return rc;
+  attach_call_err(ctx, t.p);
   gbs::PackJob job;
   job.counts = counts;
   job.n = n;
@@ -568,8 +639,15 @@ int gb_scan_reduce_then_scan(int dtype, int op, int inclusive, const void* in, v
 size_t gb_temp_storage_bytes(int kind, int dtype, int lanes, int64_t rows, int64_t cols) {
   if (!dtype_size(dtype) || lanes < 1 || lanes > kMaxLanes || rows < 0 || cols < 0) return 0;
   switch (kind) {
-    case GB_KIND_SCAN:
-      return scan_temp(dtype, 1, rows, lanes);
+    case GB_KIND_SCAN: {
+      // Two lanes of an integer type may be affine maps (GB_AFFINE): cover that too.
+      const size_t s = scan_temp(dtype, 1, rows, lanes);
+      if (lanes == 2 && is_int(dtype)) {
+        const size_t a = affine_temp(dtype, rows);
+        return a > s ? a : s;
+      }
+      return s;
+    }
     case GB_KIND_BATCHED_AXIS1:
       return scan_temp(dtype, rows, cols, lanes);
     case GB_KIND_BATCHED_AXIS0:
@@ -608,16 +686,26 @@ int gb_device_error(void* stream) {
   cudaError_t e = cudaStreamSynchronize(ctx.stream);
   if (e != cudaSuccess) return cuda_fail(e);
   unsigned bits = 0;
-  e = cudaMemcpy(&bits, ctx.err, sizeof(bits), cudaMemcpyDeviceToHost);
+  e = cudaMemcpy(&bits, ctx.err.dev, sizeof(bits), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e);
   if (bits) {
-    e = cudaMemset(ctx.err, 0, sizeof(unsigned));
+    e = cudaMemset(ctx.err.dev, 0, sizeof(unsigned));
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  if (bits & gbs::ERRBIT_TIMEOUT) return GB_ERR_TIMEOUT;
-  if (bits & gbs::ERRBIT_RANGE) return GB_ERR_RANGE;
-  if (bits & gbs::ERRBIT_INVALID) return GB_ERR_INVALID;
-  return GB_OK;
+  return status_of_bits(bits);
+}
+
+int gb_last_device_error(void* temp, void* stream) {
+  if (!temp || (uintptr_t)temp % 256) return GB_ERR_INVALID;
+  LaunchCtx ctx;
+  int rc = make_ctx(stream, ctx);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(ctx.stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned bits = 0;
+  e = cudaMemcpy(&bits, (const char*)temp + gbs::kCallErrOffset, sizeof(bits), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return status_of_bits(bits);
 }
 
 const char* gb_status_string(int status) {

@@ -30,7 +30,7 @@ template <class T> struct CompactArgs {
   int* out_idx;
   int* out_count;
   unsigned* counter;
-  unsigned* err;
+  ErrSink err;
   int bulk_ok;
   unsigned long long wait_ns;
   long long stalled_tile;
@@ -112,8 +112,12 @@ __device__ __forceinline__ unsigned count_selected(const T* in, long long n, lon
   return cnt;
 }
 
+// Nine tiles per SM (56 registers a thread): the selection bits, the tile's place and
+// the look-back's state then stay in registers.
+constexpr int kCompactTileMinBlocks = 9;
+
 template <class T>
-__global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_kernel(CompactArgs<T> a, PackedStatus<unsigned> st) {
+__global__ void __launch_bounds__(RowsGeom<T>::NT, kCompactTileMinBlocks) compact_kernel(CompactArgs<T> a, PackedStatus<unsigned> st) {
   pdl_entry();
   using G = RowsGeom<T>;
   constexpr int NT = G::NT, NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, TILE = G::TILE;
@@ -149,36 +153,30 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_ke
   }
   if (__syncthreads_or(failed)) {
     if (tid == 0) {
-      atomicOr(a.err, ERRBIT_TIMEOUT);
+      raise_err(a.err, ERRBIT_TIMEOUT);
       mbar_wait(&s_bar, 0, a.wait_ns);
       if ((long long)t != a.stalled_tile) st.publish(t, FLAG_P, 0u);
     }
     return;
   }
 
-  // Flags, ranks within the warp, warp totals.
+  // Selection bits (a lane's 32 elements in one word) and the warp's count.  The
+  // ranks are taken from the bits after the look-back, so nothing but the one word
+  // stays live across it.
   const uint4* run = reinterpret_cast<const uint4*>(s_tile) + warp * ROUNDS * 32;
   const int run0 = warp * ROUNDS * 32 * VEC;  // tile position of the warp's first element
-  const unsigned lt = lanemask_lt();
-  unsigned bits = 0, carry = 0;
-  unsigned rank0[ROUNDS];
+  unsigned bits = 0;
 #pragma unroll
   for (int j = 0; j < ROUNDS; ++j) {
     const Vec<T> x = ld_vec<T>(run + j * 32 + lane);
-    unsigned before = 0, total = 0;
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
       const int pos = run0 + (j * 32 + lane) * VEC + e;
-      const bool s = pos < len && selects(x.v[e], a.thr, a.predmask);
-      const unsigned bal = __ballot_sync(0xffffffffu, s);
-      before += __popc(bal & lt);
-      total += __popc(bal);
-      bits |= (unsigned)s << (j * VEC + e);
+      bits |= (unsigned)(pos < len && selects(x.v[e], a.thr, a.predmask)) << (j * VEC + e);
     }
-    rank0[j] = carry + before;
-    carry += total;
   }
-  if (lane == 0) s_warp[warp] = carry;
+  const unsigned wcount = __reduce_add_sync(0xffffffffu, (unsigned)__popc(bits));
+  if (lane == 0) s_warp[warp] = wcount;
   __syncthreads();
 
   if (warp == 0) {
@@ -193,7 +191,7 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_ke
       pfx = lookback_warp<unsigned, OP_ADD, G::K>(st, 0, t, a.wait_ns, timed_out);
       if (lane == 0) {
         if (!stalled) st.publish(t, FLAG_P, pfx + agg);
-        if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+        if (timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
       }
     }
     if (lane == 0) {
@@ -206,14 +204,25 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_ke
   // Stage the selected indices at their rank in the tile (the input is no longer
   // needed: its selection bits are in registers), then store them contiguously.
   int* s_idx = reinterpret_cast<int*>(s_tile);
-  const unsigned woff = warp > 0 ? s_warp[warp - 1] : 0u;
   const unsigned base_index = (unsigned)off + (unsigned)run0;
+  const unsigned lt = lanemask_lt();
+  unsigned carry = warp > 0 ? s_warp[warp - 1] : 0u;  // the warp's first slot in the tile
 #pragma unroll
   for (int j = 0; j < ROUNDS; ++j) {
-    unsigned r = woff + rank0[j];
+    // One ballot per vector slot: lane l's selected elements in round j follow those
+    // of lanes 0 .. l-1 (all slots), in element order.
+    unsigned before = 0, total = 0;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const unsigned bal = __ballot_sync(0xffffffffu, (bits >> (j * VEC + e)) & 1u);
+      before += __popc(bal & lt);
+      total += __popc(bal);
+    }
+    unsigned r = carry + before;
 #pragma unroll
     for (int e = 0; e < VEC; ++e)
       if ((bits >> (j * VEC + e)) & 1u) s_idx[r++] = (int)(base_index + (unsigned)((j * 32 + lane) * VEC + e));
+    carry += total;
   }
   __syncthreads();
   const unsigned cnt = s_warp[NW - 1];
@@ -227,6 +236,15 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT, RowsGeom<T>::MINB) compact_ke
 // a lane's selected elements get consecutive output slots after those of the
 // lanes before it (one ballot per vector slot); the round's indices are staged in
 // shared memory and stored as one contiguous window.
+//
+// The rescan does not wait for the gather.  Once the segment's count is published,
+// warp 0 gathers the earlier counts while the other warps already re-read their
+// chunks, rank the selected elements and stage their indices in a per-warp buffer
+// of CAP entries (ranks within the warp's part need no base).  When warp 0 posts
+// the base, each warp writes out what it has staged and continues round by round;
+// a warp whose buffer fills first waits for the base.  So the latency of the
+// gather (the slowest segment's count crossing a loaded memory system) overlaps
+// the rescan instead of idling every warp of the CTA.
 template <class T> struct CompactSegArgs : SegArgsBase {
   const T* in;
   T thr;
@@ -234,17 +252,33 @@ template <class T> struct CompactSegArgs : SegArgsBase {
   int* out_count;
 };
 
+constexpr int kCompactStageCap = 1536;  // indices a warp can stage before the base is known
+
+// Acquire / release on a shared-memory flag within the CTA.
+__device__ __forceinline__ unsigned ld_acquire_cta_shared(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta_shared(unsigned* p, unsigned v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
 template <class T, int PRED, class G>
 __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegArgs<T> a, PackedStatus<unsigned> st) {
   pdl_entry();
-  constexpr int NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, CH = G::CH;
+  constexpr int NW = G::NW, ROUNDS = G::ROUNDS, VEC = G::VEC, CH = G::CH, CAP = kCompactStageCap;
+  extern __shared__ __align__(16) int compact_stage_smem[];  // NW x CAP staged indices
   __shared__ unsigned s_seg;
   __shared__ unsigned s_warp[NW];
   __shared__ unsigned s_base;
-  __shared__ int s_stage_all[NW * 32 * VEC];  // a round's indices, per warp
+  __shared__ unsigned s_ready;  // the base and the warp offsets are posted
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int* s_stage = s_stage_all + warp * 32 * VEC;
-  if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
+  int* stage = compact_stage_smem + warp * CAP;
+  if (tid == 0) {
+    s_seg = atomicAdd(a.counter, 1u);
+    s_ready = 0u;
+  }
   __syncthreads();
   const unsigned seg = s_seg;
   long long c0, c1;
@@ -256,7 +290,8 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
   if (lane == 0) s_warp[warp] = cnt;
   __syncthreads();
 
-  // Phase 2: publish the segment's count, gather the earlier counts.
+  // Phase 2 (warp 0): publish the segment's count, gather the earlier counts, post
+  // the base.  The other warps go on to phase 3 meanwhile.
   if (warp == 0) {
     block_scan_warp_totals<unsigned, OP_ADD, NW>(s_warp, lane);
     __syncwarp();
@@ -266,18 +301,29 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
     if (seg > 0) {
       bool timed_out;
       base = seg_gather<unsigned, OP_ADD, G::M>(st, 0, seg, a.wait_ns, timed_out);
-      if (lane == 0 && timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+      if (lane == 0 && timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
     }
     if (lane == 0) {
       s_base = base;
       if (seg == a.ctas - 1) *a.out_count = (int)(base + agg);
+      st_release_cta_shared(&s_ready, 1u);
     }
+    __syncwarp();
   }
-  __syncthreads();
 
   // Phase 3: rescan from L2 and write the selected indices (positions fit 32 bits:
-  // compaction inputs hold fewer than 2^31 elements).
-  unsigned off = s_base + (warp > 0 ? s_warp[warp - 1] : 0u);
+  // compaction inputs hold fewer than 2^31 elements).  Until the base is posted the
+  // indices go to the warp's buffer at staged + rank.
+  bool ready = false;
+  unsigned off = 0, staged = 0;
+  // Takes the posted base: writes out the staged indices and returns the next slot.
+  auto take_base = [&]() {
+    off = s_base + (warp > 0 ? s_warp[warp - 1] : 0u);
+    for (unsigned k = lane; k < staged; k += 32) a.out_idx[off + k] = stage[k];
+    off += staged;
+    ready = true;
+    __syncwarp();  // the buffer is free again
+  };
   const unsigned long long drop = l2_policy_evict_first();
   const unsigned lt = lanemask_lt();
   const unsigned n32 = (unsigned)a.n;
@@ -300,22 +346,65 @@ __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegA
         total += __popc(bal);
         sel |= (unsigned)s << e;
       }
-      // Stage the round's indices at their ranks, then store the round's contiguous
-      // output window with consecutive lanes on consecutive slots (whole lines, not
-      // 4-byte pieces spread over 32 x VEC slots).
-      if (total != 0) {  // warp-uniform
-        __syncwarp();
-        unsigned r = before;
+      if (total == 0) continue;  // warp-uniform
+      if (!ready) {
+        // One lane reads the flag for the warp, so every lane takes the same branch.
+        unsigned posted = 0;
+        if (lane == 0) posted = ld_acquire_cta_shared(&s_ready);
+        if (__shfl_sync(0xffffffffu, posted, 0)) take_base();
+      }
+      if (!ready && staged + total > (unsigned)CAP) {
+        // The buffer is full: wait for the base (warp 0 always posts it, after at
+        // most its bounded gather; the wait is bounded too, and a warp that still
+        // sees no base drops its indices rather than write at an unknown offset).
+        const unsigned long long t0 = globaltimer();
+        unsigned posted = 0;
+        for (int spins = 0;; ++spins) {
+          if (lane == 0) posted = ld_acquire_cta_shared(&s_ready);
+          posted = __shfl_sync(0xffffffffu, posted, 0);
+          if (posted || globaltimer() - t0 > 2 * a.wait_ns) break;
+          backoff(spins);
+        }
+        if (!posted) {
+          if (lane == 0) raise_err(a.err, ERRBIT_TIMEOUT);
+          return;
+        }
+        take_base();
+      }
+      // Stage the round's indices at their ranks, then (once the base is known)
+      // store the round's contiguous output window with consecutive lanes on
+      // consecutive slots (whole lines, not 4-byte pieces spread over 32 x VEC slots).
+      int* dst = ready ? stage : stage + staged;
+      unsigned r = before;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-          if ((sel >> e) & 1u) s_stage[r++] = (int)(p0 + e);
-        __syncwarp();
-        for (unsigned k = lane; k < total; k += 32) a.out_idx[off + k] = s_stage[k];
+      for (int e = 0; e < VEC; ++e)
+        if ((sel >> e) & 1u) dst[r++] = (int)(p0 + e);
+      __syncwarp();
+      if (ready) {
+        for (unsigned k = lane; k < total; k += 32) a.out_idx[off + k] = stage[k];
         off += total;
+        __syncwarp();  // the round's reads of the buffer are done before the next writes
+      } else {
+        staged += total;
       }
     }
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) x[j] = y[j];
+  }
+  if (!ready && staged > 0) {  // the part ended before the base was posted
+    const unsigned long long t0 = globaltimer();
+    unsigned posted = 0;
+    for (int spins = 0;; ++spins) {
+      if (lane == 0) posted = ld_acquire_cta_shared(&s_ready);
+      posted = __shfl_sync(0xffffffffu, posted, 0);
+      if (posted || globaltimer() - t0 > 2 * a.wait_ns) break;
+      backoff(spins);
+    }
+    if (!posted) {
+      if (lane == 0) raise_err(a.err, ERRBIT_TIMEOUT);
+      return;
+    }
+    take_base();
   }
 }
 
@@ -347,9 +436,13 @@ cudaError_t launch_compact_seg_p(const CompactJob& job, const LaunchCtx& ctx) {
   a.out_idx = job.out_idx;
   a.out_count = job.out_count;
   PackedStatus<unsigned> st = seg_status<unsigned>(job.temp);
+  auto kern = compact_seg_kernel<T, PRED, G>;
+  const size_t smem = (size_t)G::NW * kCompactStageCap * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   profile_before(ctx);
-  cudaError_t e = clear_status(job.temp, seg_reset_bytes<unsigned>(), nullptr, 0, ctx);
-  if (e == cudaSuccess) e = launch_pdl(compact_seg_kernel<T, PRED, G>, p.ctas, G::NT, 0, ctx.stream, a, st);
+  e = clear_status(job.temp, seg_reset_bytes<unsigned>(), nullptr, 0, ctx);
+  if (e == cudaSuccess) e = launch_pdl(kern, p.ctas, G::NT, smem, ctx.stream, a, st);
   profile_after(ctx);
   return e;
 }

@@ -5,5 +5,12 @@
 #include "segmented.cuh"
 #include "rts.cuh"
 #include "scan.cuh"
+#include "scan_affine.cuh"
 
 GBS_INSTANTIATE(uint64_t)
+
+// Composition of affine maps: the signed type of the same width shares these.
+namespace gbs {
+template size_t affine_temp_bytes<uint64_t>(long long);
+template cudaError_t launch_affine<uint64_t>(const ScanJob&, const LaunchCtx&);
+}

@@ -10,10 +10,31 @@
 
 namespace gbs {
 
+// Where kernels report a device-side error (a wait that ran out, a packing total
+// over capacity, a negative count): the device's sticky word, read and cleared by
+// gb_device_error, and the call's own word in its scratch header (nullable), read
+// by gb_last_device_error.  The call's word is cleared with the rest of the header
+// by the call's status clear, so it holds what this call found and nothing older.
+struct ErrSink {
+  unsigned* dev = nullptr;
+  unsigned* call = nullptr;
+};
+
+// Byte offset of the call's error word in the scratch header (kHeaderBytes below);
+// the tile-claim counter is at offset 0.
+constexpr size_t kCallErrOffset = 128;
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void raise_err(const ErrSink& e, unsigned bits) {
+  atomicOr(e.dev, bits);
+  if (e.call) atomicOr(e.call, bits);
+}
+#endif
+
 // Settings the C ABI attaches to every launch.
 struct LaunchCtx {
   cudaStream_t stream = nullptr;
-  unsigned* err = nullptr;             // sticky device error word of this device
+  ErrSink err;                         // device-wide and per-call error words
   unsigned long long wait_ns = 0;      // limit of every in-kernel wait
   long long stalled_tile = -1;         // fault injection: tile that never publishes
   cudaEvent_t ev_before = nullptr;     // optional events around the main kernel
@@ -105,6 +126,11 @@ template <class T> size_t rts_temp_bytes(long long n, int num_sms);
 template <class T> cudaError_t launch_rts(const RtsJob& job, const LaunchCtx& ctx);
 size_t pack_temp_bytes(long long n);
 cudaError_t launch_pack(const PackJob& job, const LaunchCtx& ctx);
+// Composition of affine maps (scan_affine.cuh): T is uint32_t or uint64_t, the job
+// one row (B = 1) of R maps stored as C = 2 values each.  Instantiated in
+// inst_u32.cu / inst_u64.cu.
+template <class T> size_t affine_temp_bytes(long long n);
+template <class T> cudaError_t launch_affine(const ScanJob& job, const LaunchCtx& ctx);
 
 // Launches `kernel` with programmatic stream serialization, so that it may be
 // scheduled while the previous grid in the stream still runs; the kernel must begin

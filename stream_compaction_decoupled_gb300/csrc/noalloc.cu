@@ -53,7 +53,10 @@ int scratch_address(void** out) {
 
 extern "C" int gb_scan_inclusive_noalloc(int dtype, int op, const void* in, void* out, int64_t n,
                                          void* stream) {
-  if (n < 0) return GB_ERR_INVALID;
+  // The same argument checks as gb_scan_inclusive, in the same order: a bad type or
+  // operator is refused even when there is nothing to scan.
+  if (n < 0 || gb_temp_storage_bytes(GB_KIND_SCAN, dtype, 1, 1, 0) == 0) return GB_ERR_INVALID;
+  if (op != GB_ADD && op != GB_MAX && op != GB_MIN && op != GB_MUL) return GB_ERR_INVALID;
   if (n == 0) return GB_OK;
   const size_t need = gb_temp_storage_bytes(GB_KIND_SCAN, dtype, 1, n, 0);
   if (need == 0) return GB_ERR_INVALID;

@@ -27,7 +27,7 @@ struct PackArgs {
   long long capacity;
   int* out_total;
   unsigned* counter;
-  unsigned* err;
+  ErrSink err;
   int bulk_ok;           // counts 16-byte aligned
   int offsets_vec_ok;    // offsets 16-byte aligned
   unsigned long long wait_ns;
@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) pack_kernel(PackArgs a, Packed
   }
   if (__syncthreads_or(failed)) {
     if (tid == 0) {
-      atomicOr(a.err, ERRBIT_TIMEOUT);
+      raise_err(a.err, ERRBIT_TIMEOUT);
       mbar_wait(&s_bar, 0, a.wait_ns);
       if ((long long)t != a.stalled_tile) st.publish(t, FLAG_P, 0u);
     }
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) pack_kernel(PackArgs a, Packed
       negative = true;
     }
   }
-  if (negative) atomicOr(a.err, ERRBIT_INVALID);
+  if (negative) raise_err(a.err, ERRBIT_INVALID);
   __syncwarp();
 
   unsigned pre[ROUNDS];
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) pack_kernel(PackArgs a, Packed
       pfx = lookback_warp<unsigned, OP_SATADD, G::K>(st, 0, t, a.wait_ns, timed_out);
       if (lane == 0) {
         if (!stalled) st.publish(t, FLAG_P, Op<unsigned, OP_SATADD>::f(pfx, agg));
-        if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+        if (timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
       }
     }
     if (lane == 0) {
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) pack_kernel(PackArgs a, Packed
       if (t == a.num_tiles - 1) {
         const unsigned total = Op<unsigned, OP_SATADD>::f(pfx, agg);
         *a.out_total = total >= 0x80000000u ? 0x7fffffff : (int)total;
-        if (total >= 0x80000000u || (long long)total > a.capacity) atomicOr(a.err, ERRBIT_RANGE);
+        if (total >= 0x80000000u || (long long)total > a.capacity) raise_err(a.err, ERRBIT_RANGE);
       }
     }
   }
@@ -281,14 +281,14 @@ __global__ void __launch_bounds__(PackSegGeom::NT, PackSegGeom::MINB) pack_seg_k
     if (seg > 0) {
       bool timed_out;
       base = seg_gather<unsigned, OP_SATADD, G::M>(st, 0, seg, a.wait_ns, timed_out);
-      if (lane == 0 && timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+      if (lane == 0 && timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
     }
     if (lane == 0) {
       s_base = base;
       if (seg == a.ctas - 1) {
         const unsigned total = Op<unsigned, OP_SATADD>::f(base, agg);
         *a.out_total = total >= CAP ? 0x7fffffff : (int)total;
-        if (total >= CAP || (long long)total > a.capacity) atomicOr(a.err, ERRBIT_RANGE);
+        if (total >= CAP || (long long)total > a.capacity) raise_err(a.err, ERRBIT_RANGE);
       }
     }
   }
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(PackSegGeom::NT, PackSegGeom::MINB) pack_seg_k
     }
     run = cend_u;
   }
-  if (negative) atomicOr(a.err, ERRBIT_INVALID);
+  if (negative) raise_err(a.err, ERRBIT_INVALID);
 }
 
 size_t pack_temp_bytes(long long n) {

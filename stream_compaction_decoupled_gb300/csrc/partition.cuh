@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) partition_seg_kernel(Partition
     const unsigned base = seg > 0 ? seg_gather<unsigned, OP_ADD, G::M>(st, 0, seg, a.wait_ns, t1) : 0u;
     const unsigned total = seg_gather<unsigned, OP_ADD, G::M>(st, 0, a.ctas, a.wait_ns, t2);
     if (lane == 0) {
-      if (t1 || t2) atomicOr(a.err, ERRBIT_TIMEOUT);
+      if (t1 || t2) raise_err(a.err, ERRBIT_TIMEOUT);
       s_base = base;
       s_total = total;
       if (seg == a.ctas - 1) *a.out_count = (int)total;

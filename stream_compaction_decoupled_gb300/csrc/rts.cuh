@@ -40,7 +40,7 @@ template <class T> struct RtsArgs {
   T init;
   int inclusive;
   int vec_ok;           // in and out 16-byte aligned
-  unsigned* err;
+  ErrSink err;
   unsigned long long wait_ns;
 };
 
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(RowsGeom<T>::NT) rts_scan_kernel(RtsArgs<T> a)
     }
     if (__syncthreads_or(failed)) {
       if (tid == 0) {
-        atomicOr(a.err, ERRBIT_TIMEOUT);
+        raise_err(a.err, ERRBIT_TIMEOUT);
         mbar_wait(&s_bar[q], (unsigned)((k >> 1) & 1), a.wait_ns);
         if (k + 1 < ntiles) mbar_wait(&s_bar[q ^ 1], (unsigned)(((k + 1) >> 1) & 1), a.wait_ns);
       }
@@ -307,7 +307,8 @@ template <class T, int OP> cudaError_t launch_rts_op(const RtsJob& job, const La
   // The three launches follow one another with programmatic dependent launch; the
   // profile events (when set) bracket all three.
   profile_before(ctx);
-  cudaError_t e = launch_pdl(rts_reduce_kernel<T, OP>, a.nblocks, 256, 0, ctx.stream, a);
+  cudaError_t e = clear_status(job.temp, kHeaderBytes, nullptr, 0, ctx);  // the call's error word
+  if (e == cudaSuccess) e = launch_pdl(rts_reduce_kernel<T, OP>, a.nblocks, 256, 0, ctx.stream, a);
   if (e == cudaSuccess)
     e = launch_pdl(rts_spine_kernel<T, OP>, 1, kRtsMaxBlocks, 0, ctx.stream, a.partials, a.nblocks);
   if (e == cudaSuccess) e = launch_pdl(rts_scan_kernel<T, OP, false>, a.nblocks, RowsGeom<T>::NT, 0, ctx.stream, a);
@@ -337,7 +338,8 @@ template <class T, int OP> cudaError_t launch_stf_op(const RtsJob& job, const La
   a.err = ctx.err;
   a.wait_ns = ctx.wait_ns;
   profile_before(ctx);
-  cudaError_t e = launch_pdl(rts_scan_kernel<T, OP, true>, a.nblocks, RowsGeom<T>::NT, 0, ctx.stream, a);
+  cudaError_t e = clear_status(job.temp, kHeaderBytes, nullptr, 0, ctx);  // the call's error word
+  if (e == cudaSuccess) e = launch_pdl(rts_scan_kernel<T, OP, true>, a.nblocks, RowsGeom<T>::NT, 0, ctx.stream, a);
   if (e == cudaSuccess)
     e = launch_pdl(rts_spine_kernel<T, OP>, 1, kRtsMaxBlocks, 0, ctx.stream, a.partials, a.nblocks);
   if (e == cudaSuccess) e = launch_pdl(stf_fan_kernel<T, OP>, a.nblocks, 256, 0, ctx.stream, a);

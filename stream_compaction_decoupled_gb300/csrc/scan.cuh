@@ -42,12 +42,14 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
       }
     }
   }
-  if (seg_applies<T>(job)) {
-    switch (job.op) {
-      case OP_ADD: return launch_seg_op<T, OP_ADD>(job, ctx);
-      case OP_MAX: return launch_seg_op<T, OP_MAX>(job, ctx);
-      case OP_MUL: return launch_seg_op<T, OP_MUL>(job, ctx);
-      default: return launch_seg_op<T, OP_MIN>(job, ctx);
+  if constexpr (!std::is_same<T, double>::value) {  // fp64 takes the chunked variant above
+    if (seg_applies<T>(job)) {
+      switch (job.op) {
+        case OP_ADD: return launch_seg_op<T, OP_ADD>(job, ctx);
+        case OP_MAX: return launch_seg_op<T, OP_MAX>(job, ctx);
+        case OP_MUL: return launch_seg_op<T, OP_MUL>(job, ctx);
+        default: return launch_seg_op<T, OP_MIN>(job, ctx);
+      }
     }
   }
   if (job.C == 1 && stash_applies<T>(job, ctx.num_sms)) {

@@ -29,7 +29,7 @@ template <class T> struct LanesArgs {
   unsigned tiles_per_chain; // ceil(R / RT)
   unsigned num_tiles;       // B * strips * tiles_per_chain
   unsigned* counter;
-  unsigned* err;
+  ErrSink err;
   const T* init;            // device copy of the initial value (exclusive)
   int init_lanes;           // lane c starts from init[c % init_lanes]
   int inclusive;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(Gm::NT) scan_lanes_kernel(LanesArgs<T> a, S st
   }
   if (__syncthreads_or(failed)) {
     if (tid == 0) {
-      atomicOr(a.err, ERRBIT_TIMEOUT);
+      raise_err(a.err, ERRBIT_TIMEOUT);
       mbar_wait(&s_bar, 0, a.wait_ns);
     }
     if (tid < cols && (long long)t != a.stalled_tile) st.publish((long long)t * CT + tid, FLAG_P, T{});
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(Gm::NT) scan_lanes_kernel(LanesArgs<T> a, S st
       const T pfx = lookback_lane<T, OP, Gm::D>(st, first, tt, tid, CT, a.wait_ns, timed_out);
       if (!stalled) st.publish(si, FLAG_P, Op<T, OP>::f(pfx, agg));
       s_pfx[tid] = pfx;
-      if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+      if (timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
     }
   }
   __syncthreads();

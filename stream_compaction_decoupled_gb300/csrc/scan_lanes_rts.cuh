@@ -43,7 +43,7 @@ template <class T> struct LanesRtsArgs {
   const T* init;             // device copy of the initial values (exclusive)
   int init_lanes;            // lane c starts from init[c % init_lanes]
   int inclusive;
-  unsigned* err;
+  ErrSink err;
   unsigned long long wait_ns;
   T* gp;                     // [tiles][G][CT]: group partials (fp64), else null
 };
@@ -147,7 +147,7 @@ template <class T>
 __device__ __forceinline__ void lanes_stage_abort(const LanesRtsArgs<T>& a, unsigned chain, unsigned tt, unsigned t1,
                                                   const T* out, unsigned long long* bars, unsigned phases, int q) {
   if (threadIdx.x != 0) return;
-  atomicOr(a.err, ERRBIT_TIMEOUT);
+  raise_err(a.err, ERRBIT_TIMEOUT);
   mbar_wait(&bars[q], ((phases >> q) & 1u) ^ 1u, a.wait_ns);  // the phase that did not complete
   if (tt + 1 < t1 && lanes_tile_bulk(a, lanes_tile_at(a, chain, tt + 1), out))
     mbar_wait(&bars[q ^ 1], (phases >> (q ^ 1)) & 1u, a.wait_ns);
@@ -519,8 +519,8 @@ cudaError_t launch_lanes_rts_op(const ScanJob& job, const LaunchCtx& ctx) {
   a.wait_ns = ctx.wait_ns;
   const unsigned ranges = p.chains * p.K;
   profile_before(ctx);
-  cudaError_t e = cudaSuccess;
-  if (!job.inclusive)
+  cudaError_t e = clear_status(job.temp, kHeaderBytes, nullptr, 0, ctx);  // the call's error word
+  if (e == cudaSuccess && !job.inclusive)
     e = cudaMemcpyAsync(init_area, job.init_host, (size_t)job.init_lanes * sizeof(T), cudaMemcpyHostToDevice,
                         ctx.stream);
   if (e == cudaSuccess) e = launch_pdl(lanes_rts_reduce_kernel<T, OP, Gm>, ranges, Gm::NT, 0, ctx.stream, a);

@@ -29,7 +29,7 @@ template <class T> struct RowsArgs {
   unsigned tiles_per_row;   // ceil(R / TILE)
   unsigned num_tiles;       // rows * tiles_per_row
   unsigned* counter;        // tile-claim counter, 0 on entry
-  unsigned* err;            // sticky device error word
+  ErrSink err;            // device-wide and per-call error words
   T init;                   // exclusive scans: folded in on the left of every row
   int inclusive;
   int bulk_ok;              // in, out and every row start are 16-byte aligned
@@ -50,15 +50,18 @@ template <class T, int NT_, int ROUNDS_, int K_, int MINB_> struct RowsCfg {
 };
 
 // The configuration the library uses: 16 KB tiles of 128 threads, so that a dozen
-// CTAs (tiles) are resident per SM, and a look-back window of 32 x 2 tiles.  (A
-// sweep on the fp32 1e8 scan: windows of 4 or 8 tiles per lane were slower, 6 CTAs
-// of 256 threads were slower, 32 KB tiles were no faster.)
+// CTAs (tiles) are resident per SM, and a look-back window of 32 tiles (one per
+// lane).  (A sweep on the fp32 1e8 scan: windows of 4 or 8 tiles per lane were
+// slower, 6 CTAs of 256 threads were slower, 32 KB tiles were no faster.  A window
+// of 2 tiles per lane made warp 0 spill its per-round prefixes at the 40 registers
+// that 12 CTAs leave a thread.)  8-byte integers get 10 CTAs (48 registers), whose
+// pairs of registers per value would spill at 40.
 // fp64 runs the chunked variant (see scan_rows_chunk_kernel), which keeps a thread's
 // 16 doubles in registers; 8 CTAs per SM (64 registers a thread) let one tile's
 // FP64 adds overlap other tiles' loads and look-backs best (113 us against 130 us
 // at 4 CTAs for 1e7 doubles).
 template <class T>
-using RowsGeom = RowsCfg<T, 128, 8, 2, std::is_same<T, double>::value ? 8 : 12>;
+using RowsGeom = RowsCfg<T, 128, 8, 1, std::is_same<T, double>::value ? 8 : (sizeof(T) == 8 ? 10 : 12)>;
 
 template <class T, int OP, class G, class S>
 __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_kernel(RowsArgs<T> a, S st) {
@@ -103,7 +106,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_kernel(RowsArgs<T> a
   if (__syncthreads_or(failed)) {
     // The copy never landed: record it, let successors go on, write nothing.
     if (tid == 0) {
-      atomicOr(a.err, ERRBIT_TIMEOUT);
+      raise_err(a.err, ERRBIT_TIMEOUT);
       mbar_wait(&s_bar, 0, a.wait_ns);  // give the copy in flight one more bounded wait
       if ((long long)t != a.stalled_tile) {
         S(st).publish((long long)row * a.tiles_per_row + tt, FLAG_P, T{});
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_kernel(RowsArgs<T> a
         if (!stalled) st.publish(first + tt, FLAG_P, Op<T, OP>::f(pfx, agg));
         s_prefix = pfx;
         s_has_prefix = 1;
-        if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+        if (timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
       }
     }
   }
@@ -217,24 +220,29 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_chunk_kernel(RowsArg
   }
   if (__syncthreads_or(failed)) {
     if (tid == 0) {
-      atomicOr(a.err, ERRBIT_TIMEOUT);
+      raise_err(a.err, ERRBIT_TIMEOUT);
       mbar_wait(&s_bar, 0, a.wait_ns);
       if ((long long)t != a.stalled_tile) st.publish((long long)row * a.tiles_per_row + tt, FLAG_P, T{});
     }
     return;
   }
 
-  // Pass 1: the thread's chunk total, then one warp scan of the totals.
+  // Pass 1: the thread's chunk total, then one warp scan of the totals.  The chunk
+  // is read again from shared memory in pass 2, so it does not occupy registers
+  // across the look-back.
   uint4* chunk = reinterpret_cast<uint4*>(s_tile) + (warp * 32 + lane) * CV;
-  Vec<T> v[CV];
-  chunk_load<T, CV>(chunk, lane, v);
-  T tot = v[0].v[0];  // any order: the total does not depend on it (up to rounding)
+  T tot;
+  {
+    Vec<T> v[CV];
+    chunk_load<T, CV>(chunk, lane, v);
+    tot = v[0].v[0];  // any order: the total does not depend on it (up to rounding)
 #pragma unroll
-  for (int e = 1; e < VEC; ++e) tot = Op<T, OP>::f(tot, v[0].v[e]);
+    for (int e = 1; e < VEC; ++e) tot = Op<T, OP>::f(tot, v[0].v[e]);
 #pragma unroll
-  for (int j = 1; j < CV; ++j)
+    for (int j = 1; j < CV; ++j)
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) tot = Op<T, OP>::f(tot, v[j].v[e]);
+      for (int e = 0; e < VEC; ++e) tot = Op<T, OP>::f(tot, v[j].v[e]);
+  }
   const T wi = warp_inclusive<T, OP>(tot, lane);
   const T we = __shfl_up_sync(0xffffffffu, wi, 1);  // lane 0: none
   if (lane == 31) s_warp[warp] = wi;
@@ -257,7 +265,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_chunk_kernel(RowsArg
         if (!stalled) st.publish(first + tt, FLAG_P, Op<T, OP>::f(pfx, agg));
         s_prefix = pfx;
         s_has_prefix = 1;
-        if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+        if (timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
       }
     }
   }
@@ -279,6 +287,8 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_rows_chunk_kernel(RowsArg
     base = hb ? Op<T, OP>::f(a.init, base) : a.init;
     hb = true;
   }
+  Vec<T> v[CV];
+  chunk_load<T, CV>(chunk, lane, v);
   chunk_rotate<T, CV, -1>(v, lane);  // v[k] is now chunk vector k
   if (a.inclusive) {
 #pragma unroll

@@ -45,7 +45,9 @@ template <class T, int NT_, int ROUNDS_, int MINB_> struct SegCfg {
   static constexpr int MAXSEG = 512;            // segments (CTAs) per launch at most
   static constexpr int M = MAXSEG / 32;         // earlier aggregates per lane in phase 2
 };
-template <class T> using SegGeom = SegCfg<T, 1024, 4, 1>;
+// 8-byte elements take 2 rounds a chunk (the chunk and the one prefetched behind it
+// then fit the 64 registers a thread of a 1024-thread CTA has).
+template <class T> using SegGeom = SegCfg<T, 1024, sizeof(T) == 8 ? 2 : 4, 1>;
 
 // Work split of `rows` independent rows of n elements (a 1-D scan is one row): each
 // row's nc chunks are spread over `segs` segments (CTAs; segment p of a row takes
@@ -86,7 +88,7 @@ struct SegArgsBase {
   unsigned segs;
   unsigned ctas;
   unsigned* counter;
-  unsigned* err;
+  ErrSink err;
   unsigned long long wait_ns;
   long long stalled;  // fault injection: this segment never publishes
 };
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, 
     if (part > 0) {
       bool timed_out;
       gathered = seg_gather<T, OP, G::M>(st, seg - part, part, a.wait_ns, timed_out);
-      if (lane == 0 && timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+      if (lane == 0 && timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
     }
     if (lane == 0) {
       T b{};
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_chunk_kernel(SegArgs<
     if (seg > 0) {
       bool timed_out;
       gathered = seg_gather<T, OP, G::M>(st, 0, seg, a.wait_ns, timed_out);
-      if (lane == 0 && timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+      if (lane == 0 && timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
     }
     if (lane == 0) {
       T b{};

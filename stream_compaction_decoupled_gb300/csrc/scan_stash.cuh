@@ -89,7 +89,7 @@ template <class T> struct StashArgs {
   unsigned num_tiles;  // ceil(n / TILE)
   unsigned num_runs;   // ceil(num_tiles / RUN)
   unsigned* counter;   // run-claim counter, 0 on entry
-  unsigned* err;
+  ErrSink err;
   T init;
   int inclusive;
   unsigned long long wait_ns;
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(C::NT, 1) scan_stash_kernel(StashArgs<T> a, S 
     return a.n - off >= TILE ? TILE : (int)(a.n - off);
   };
   auto fail = [&]() {
-    atomicOr(a.err, ERRBIT_TIMEOUT);
+    raise_err(a.err, ERRBIT_TIMEOUT);
     sh.abort = 1;
   };
 
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(C::NT, 1) scan_stash_kernel(StashArgs<T> a, S 
         pfx = lookback_warp<T, OP, C::K>(st, 0, r, a.wait_ns, timed_out);
         if (lane == 0) {
           if ((long long)r != a.stalled_run) st.publish(r, FLAG_P, Op<T, OP>::f(pfx, agg));
-          if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+          if (timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
         }
       }
       if (lane == 0) {

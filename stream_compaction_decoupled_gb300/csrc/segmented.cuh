@@ -21,8 +21,9 @@ namespace gbs {
 
 enum : unsigned { FLAG_HEAD = 4u };
 
+// 8-byte values: one CTA per SM, so a lane's 8 values and flags stay in registers.
 template <class T> struct SegmentedCfg {
-  static constexpr int NT = 512, NW = NT / 32, MINB = 2;
+  static constexpr int NT = 512, NW = NT / 32, MINB = sizeof(T) == 8 ? 1 : 2;
   static constexpr int K = 64 / (int)sizeof(T);  // elements per lane per chunk: 64 bytes
   static constexpr int CH = 32 * K;
   static constexpr int MAXSEG = 512, M = MAXSEG / 32;
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_segmented_kernel(Segmente
     bool bf = false, timed_out = false;
     if (seg > 0) seg_gather_pair<T, OP, G::M>(st, seg, a.wait_ns, bv, bf, timed_out);
     if (lane == 0) {
-      if (timed_out) atomicOr(a.err, ERRBIT_TIMEOUT);
+      if (timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
       s_bv = bv;
       s_bf = bf;
       s_bhas = seg > 0;

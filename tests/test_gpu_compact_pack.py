@@ -46,6 +46,19 @@ def test_compact_small(dt, n, pred):
     check_compact(x, pred, thr, "%s n=%d %s" % (np.dtype(dt).name, n, pred))
 
 
+@pytest.mark.parametrize("dt", [np.uint32, np.uint64])
+@pytest.mark.parametrize("n", [4097, 1_000_003])
+@pytest.mark.parametrize("pred", ["lt", "gt", "le"])
+def test_compact_unsigned_full_range(dt, n, pred):
+    """Unsigned comparisons on values with the top bit set, against a threshold that
+    has it too: a signed comparison would select the complement of the right set."""
+    if not hasattr(torch, "uint32"):
+        pytest.skip("no torch unsigned dtypes")
+    x = workloads.full_range_uints(n, n + 3, dt)
+    thr = dt(3 * (int(np.iinfo(dt).max) // 4))
+    check_compact(x, pred, thr, "%s n=%d %s full range" % (np.dtype(dt).name, n, pred))
+
+
 def test_compact_none_all_and_empty():
     x = workloads.uniform01(3 * 4096 + 5, np.float32, 3)
     check_compact(x, "lt", 0.0, "none")

@@ -61,8 +61,9 @@ def scan_values(dt, op, n, seed):
         return workloads.odd_ints(n, seed, np.int64).astype(NP[dt])
     if dt[0] == "f":
         return workloads.normal(n, NP[dt], seed)
-    lo = 0 if dt[0] == "u" else -1000
-    return workloads.small_ints(n, seed, lo, 1000, dtype=np.int64).astype(NP[dt])
+    if dt[0] == "u":  # the whole range: max/min must compare as unsigned, add wraps
+        return workloads.full_range_uints(n, seed, NP[dt])
+    return workloads.small_ints(n, seed, -1000, 1000, dtype=np.int64).astype(NP[dt])
 
 
 def draw_init(r, x, op, inclusive):
@@ -150,11 +151,13 @@ PREDS = ["lt", "le", "gt", "ge", "eq", "ne"]
 def select_values(dt, n, seed):
     if dt[0] == "f":
         return workloads.uniform01(n, NP[dt], seed)
+    if dt[0] == "u" and seed % 2:  # the whole range: comparisons must be unsigned
+        return workloads.full_range_uints(n, seed, NP[dt])
     return workloads.small_ints(n, seed, 0, 100, dtype=np.int64).astype(NP[dt])
 
 
 def draw_threshold(r, dt, x, pred):
-    if pred in ("eq", "ne") and x.size:
+    if (pred in ("eq", "ne") or (dt[0] == "u" and x.size and int(x.max()) > 100)) and x.size:
         return x[int(r.integers(0, x.size))]
     return float(r.random()) if dt[0] == "f" else int(r.integers(0, 101))
 

@@ -28,8 +28,8 @@ def _cuda():
 def make(dt, n, seed):
     if dt.startswith("f"):
         return workloads.normal(n, NP[dt], seed)
-    if dt.startswith("u"):
-        return workloads.small_ints(n, seed, 0, 1000, dtype=NP[dt])
+    if dt.startswith("u"):  # the whole range: max/min must compare as unsigned
+        return workloads.full_range_uints(n, seed, NP[dt])
     return workloads.small_ints(n, seed, -1000, 1000, dtype=NP[dt])
 
 

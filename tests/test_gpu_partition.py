@@ -36,6 +36,11 @@ def make(dt, n, seed):
     return workloads.small_ints(n, seed, 0, 1000, dtype=np.int64).astype(NP[dt])
 
 
+def make_full(dt, n, seed):
+    """Unsigned values over the whole range (about half with the top bit set)."""
+    return workloads.full_range_uints(n, seed, NP[dt])
+
+
 def check(x, pred, thr, res, what, with_idx=True):
     out, out_idx, cnt = res
     vals, idx, m = oracle.partition(x, pred, thr)
@@ -75,6 +80,19 @@ def test_partition_predicates_and_selectivity(dt, pred, thr):
     if dt[0] == "f":
         x = np.floor(x * 1000).astype(x.dtype)  # integral values so eq / ne select some
     check(x, pred, thr, gb.partition(dev(x), pred, thr), "%s %s %s" % (dt, pred, thr))
+
+
+@pytest.mark.parametrize("dt", ["u32", "u64"])
+@pytest.mark.parametrize("pred", ["lt", "ge", "gt"])
+@pytest.mark.parametrize("n", [4097, 1_000_003])
+def test_partition_unsigned_full_range(dt, pred, n):
+    """Unsigned comparisons on values with the top bit set, against a threshold that
+    has it too (a signed comparison would put them on the wrong side)."""
+    if not hasattr(torch, "uint32"):
+        pytest.skip("no torch unsigned dtypes")
+    x = make_full(dt, n, 40 + n % 7)
+    thr = NP[dt](3 * (int(np.iinfo(NP[dt]).max) // 4))
+    check(x, pred, thr, gb.partition(dev(x), pred, thr), "%s %s full range n=%d" % (dt, pred, n))
 
 
 @pytest.mark.parametrize("dt", ["i32", "u32", "i64", "u64"])

@@ -53,7 +53,8 @@ def test_scan_then_fan_matches(dt, op, n):
              else workloads.odd_ints(n, n, np.int64).astype(dt))
     else:
         x = (workloads.normal(n, dt, n) if np.dtype(dt).kind == "f"
-             else workloads.small_ints(n, n, 0 if np.dtype(dt).kind == "u" else -1000, 1000, dtype=dt))
+             else workloads.full_range_uints(n, n, dt) if np.dtype(dt).kind == "u"
+             else workloads.small_ints(n, n, -1000, 1000, dtype=dt))
     xd = dev(x)
     got = gb.scan_then_fan(xd, op).cpu().numpy()
     assert_scan_matches(got, as3(x, 1, n, 1), op, True, what="stf %s %s %d" % (np.dtype(dt).name, op, n))
@@ -93,7 +94,7 @@ def stall():
 
 @pytest.mark.parametrize("kind", ["rows_f32", "rows_f64", "lanes", "lanes_wide", "segments", "segments_f64",
                                   "compact_segments", "compact_tiles", "pack", "l2_resident", "partition",
-                                  "segmented"])
+                                  "segmented", "affine_segments", "affine_tiles"])
 def test_stalled_tile_times_out(stall, kind):
     n = 64 * 4096 if kind != "l2_resident" else 26_000_000
     x = workloads.uniform01(n, np.float32, 1)
@@ -119,6 +120,10 @@ def test_stalled_tile_times_out(stall, kind):
         gb.scan_segmented(dev(x), dev(workloads.head_flags(n, 0.01, 2)))
     elif kind == "partition":  # every segment waits for all counts; segment 3 never publishes
         gb.partition(dev(x), "lt", 0.5)
+    elif kind in ("affine_segments", "affine_tiles"):  # composition of affine maps, two lanes
+        xi = dev(workloads.small_ints(n, 5))
+        gb.scan_inclusive(xi if kind == "affine_segments" else dev(workloads.small_ints(n + 2, 5))[2:], "affine",
+                          lanes=2)
     elif kind == "compact_tiles":
         gb.compact(dev(np.concatenate([x[:1], x]))[1:], "lt", 0.5)
     else:
@@ -129,4 +134,64 @@ def test_stalled_tile_times_out(stall, kind):
     gb.set_wait_limit_ns(0)
     xi = workloads.small_ints(n, 2)
     assert np.array_equal(gb.scan_inclusive(dev(xi)).cpu().numpy(), oracle.scan(xi))
+    assert gb.device_error() == gb.OK
+
+
+def test_per_call_status_keeps_streams_apart(stall):
+    """gb_last_device_error(temp, stream) reads the status word in a call's own
+    scratch: a call that timed out on one stream does not show in an independent
+    call on another stream with its own scratch, and the next call with the first
+    scratch clears it.  The device-wide word sees both."""
+    n = 64 * 4096
+    x = dev(workloads.uniform01(n, np.float32, 1))
+    nbytes = gb.temp_storage_bytes(gb.KIND_SCAN, gb.F32, 1, n)
+    temp_a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    temp_b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    assert gb.device_error() == gb.OK
+    gb.set_wait_limit_ns(5_000_000)   # 5 ms
+    gb.set_stalled_tile(3)
+    gb.scan_inclusive(x, temp=temp_a)                 # segment 3 never publishes
+    torch.cuda.synchronize()
+    gb.set_stalled_tile(-1)
+    gb.set_wait_limit_ns(0)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        out_b = gb.scan_inclusive(x, temp=temp_b, stream=side)
+    assert gb.last_device_error(temp_b, side) == gb.OK
+    assert gb.last_device_error(temp_a) == gb.ERR_TIMEOUT
+    assert gb.last_device_error(temp_a) == gb.ERR_TIMEOUT   # reading does not clear it
+    assert gb.device_error() == gb.ERR_TIMEOUT              # the device-wide view
+    want = oracle.scan(x.cpu().numpy())
+    assert_scan_matches(out_b.cpu().numpy(), as3(x.cpu().numpy(), 1, n, 1), "add", True, what="side stream")
+    gb.scan_inclusive(x, temp=temp_a)                 # the next call clears the word
+    assert gb.last_device_error(temp_a) == gb.OK
+    del want
+
+
+def test_per_call_status_of_host_scan_and_comparators(stall):
+    """The host-array scan collects every chunk's status in its work area's header;
+    the three-launch comparators clear their header too."""
+    n = 8 * 65_536
+    xh = torch.from_numpy(workloads.small_ints(n, 3)).pin_memory()
+    work = torch.empty(gb.host_scan_work_bytes(torch.int32, n, 65_536), dtype=torch.uint8, device="cuda")
+    gb.set_wait_limit_ns(5_000_000)
+    gb.set_stalled_tile(0)     # segment 0 of every chunk scan never publishes
+    gb.scan_inclusive_host(xh, chunk_elems=65_536, work=work)
+    assert gb.last_device_error(work) == gb.ERR_TIMEOUT
+    assert gb.device_error() == gb.ERR_TIMEOUT
+    gb.set_stalled_tile(-1)
+    gb.set_wait_limit_ns(0)
+    out = gb.scan_inclusive_host(xh, chunk_elems=65_536, work=work)
+    assert gb.last_device_error(work) == gb.OK
+    assert np.array_equal(out.numpy(), oracle.scan(xh.numpy()))
+    xd = dev(workloads.normal(1_000_003, np.float32, 4))
+    temp = torch.empty(gb.temp_storage_bytes(gb.KIND_REDUCE_THEN_SCAN, gb.F32, 1, xd.numel()), dtype=torch.uint8,
+                       device="cuda")
+    temp.fill_(0xff)           # a stale error word must not survive the call's clear
+    gb.scan_reduce_then_scan(xd, temp=temp)
+    assert gb.last_device_error(temp) == gb.OK
+    temp.fill_(0xff)
+    gb.scan_then_fan(xd, temp=temp)
+    assert gb.last_device_error(temp) == gb.OK
     assert gb.device_error() == gb.OK

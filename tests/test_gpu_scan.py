@@ -39,8 +39,8 @@ def make(dt: str, n: int, seed: int) -> np.ndarray:
     npt = DTYPES[dt][0]
     if dt.startswith("f"):
         return workloads.normal(n, npt, seed)
-    if dt.startswith("u"):
-        return workloads.small_ints(n, seed, 0, 1000, dtype=npt)
+    if dt.startswith("u"):  # the whole range: max/min must compare as unsigned
+        return workloads.full_range_uints(n, seed, npt)
     return workloads.small_ints(n, seed, -1000, 1000, dtype=npt)
 
 
@@ -129,6 +129,26 @@ def test_library_allocated_temp():
     assert_scan_matches(to_host(out), as3(x, 1, x.size, 1), "add", True, what="temp NULL")
 
 
+def test_side_stream_calls_without_temp():
+    """Calls on a side stream with scratch chosen by the binding: it allocates the
+    scratch on that stream, so allocations on the default stream made while the call
+    runs cannot be handed the same block."""
+    side = torch.cuda.Stream()
+    x = to_dev(workloads.small_ints(3_000_017, 5, -9, 10))
+    want = to_dev(oracle.scan(x.cpu().numpy()))
+    side.wait_stream(torch.cuda.current_stream())
+    outs = []
+    for _ in range(10):
+        with torch.cuda.stream(side):
+            outs.append(gb.scan_inclusive(x, stream=side))
+        junk = torch.full((1 << 16,), -1, dtype=torch.int32, device="cuda")  # default-stream work
+        junk += 1
+    torch.cuda.synchronize()
+    for k, o in enumerate(outs):
+        assert torch.equal(o, want), "side-stream call %d differs" % k
+    assert gb.device_error() == gb.OK
+
+
 def test_argument_errors():
     lib = gb.load()
     x = torch.zeros(4096, dtype=torch.float32, device="cuda")
@@ -145,8 +165,10 @@ def test_argument_errors():
     assert gb.device_error() == gb.OK
 
 
-def test_repeated_calls_stress():
-    """Many tiles, many calls: every look-back interleaving must give the same bits."""
+def test_repeated_calls_segment_kernel():
+    """An aligned 1e7 int32 row takes the segment kernel, which has no look-back: each
+    segment gathers every earlier segment's aggregate once they are all published.
+    Thirty calls, whichever segments publish first, must give the same bits."""
     x = workloads.small_ints(10_000_000, 77, -5, 6)
     xd = to_dev(x)
     want = oracle.scan(x)
@@ -154,6 +176,47 @@ def test_repeated_calls_stress():
     for _ in range(30):
         gb.scan_inclusive(xd, out=out)
         assert np.array_equal(to_host(out), want)
+    assert gb.device_error() == gb.OK
+
+
+# ---- stress of the decoupled look-back itself (many calls, bit-exact) ----------------
+# Integer add is exact in any bracketing, so every call must give the oracle's bits
+# whatever order the tiles publish in and however far each look-back walks.
+
+@pytest.mark.parametrize("dt,n", [("i32", 3000 * 4096 + 1), ("i64", 3000 * 2048 + 1), ("i32", 300 * 4096 + 5)])
+def test_lookback_stress_row_kernel(dt, n):
+    """A view 4 bytes past a 16-byte boundary can only take the row kernel: one CTA
+    per tile (4096 four-byte or 2048 eight-byte elements), each tile's warp 0 looking
+    back over its predecessors' status words (one packed word for 4-byte values, a
+    flag and a value slot for 8-byte ones).  3000 tiles per call, 100 calls."""
+    npt = DTYPES[dt][0]
+    base = workloads.small_ints(n + 1, 91 + n % 7, -7, 8, dtype=npt)
+    want = to_dev(oracle.scan(base[1:]))
+    xd = to_dev(base)[1:]
+    out = torch.empty(n + 1, dtype=xd.dtype, device=xd.device)[1:]   # unaligned output too
+    for k in range(100):
+        gb.scan_inclusive(xd, out=out)
+        assert torch.equal(out, want), "call %d differs" % k
+    assert gb.device_error() == gb.OK
+
+
+@pytest.mark.parametrize("dt,n", [("i32", 30_000_001), ("i64", 13_000_003)])
+def test_lookback_stress_l2_resident_kernel(dt, n):
+    """An aligned row past 96 MiB takes the L2-resident kernel: persistent CTAs claim
+    runs of tiles and look back over run status words.  20 calls, in place and not."""
+    npt = DTYPES[dt][0]
+    x = workloads.small_ints(n, 92, -7, 8, dtype=npt)
+    want = to_dev(oracle.scan(x))
+    xd = to_dev(x)
+    out = torch.empty_like(xd)
+    for k in range(20):
+        if k % 4 == 3:
+            y = xd.clone()
+            gb.scan_inclusive(y, out=y)
+            assert torch.equal(y, want), "in-place call %d differs" % k
+        else:
+            gb.scan_inclusive(xd, out=out)
+            assert torch.equal(out, want), "call %d differs" % k
     assert gb.device_error() == gb.OK
 
 

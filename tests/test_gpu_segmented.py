@@ -36,8 +36,9 @@ def values(dt, op, n, seed):
         return workloads.odd_ints(n, seed, np.int64).astype(NP[dt])
     if dt[0] == "f":
         return workloads.normal(n, NP[dt], seed)
-    lo = 0 if dt[0] == "u" else -1000
-    return workloads.small_ints(n, seed, lo, 1000, dtype=np.int64).astype(NP[dt])
+    if dt[0] == "u":  # the whole range: max/min must compare as unsigned
+        return workloads.full_range_uints(n, seed, NP[dt])
+    return workloads.small_ints(n, seed, -1000, 1000, dtype=np.int64).astype(NP[dt])
 
 
 def check(got, x, fl, op, inclusive, init, what):

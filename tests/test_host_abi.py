@@ -31,7 +31,8 @@ def test_header_declares_the_api():
     names = declared_functions()
     for need in ("gb_scan_inclusive", "gb_scan_exclusive", "gb_scan_batched", "gb_compact",
                  "gb_partition", "gb_scan_segmented", "gb_pack_by_counts", "gb_scan_reduce_then_scan",
-                 "gb_scan_then_fan", "gb_temp_storage_bytes", "gb_device_error", "gb_status_string"):
+                 "gb_scan_then_fan", "gb_temp_storage_bytes", "gb_device_error", "gb_last_device_error",
+                 "gb_status_string"):
         assert need in names
 
 
@@ -51,7 +52,8 @@ def test_c_translation_unit_compiles_against_header(tmp_path):
                  ' (void)gb_scan_inclusive; (void)gb_scan_exclusive; (void)gb_scan_batched;\n'
                  ' (void)gb_compact; (void)gb_pack_by_counts; (void)gb_scan_reduce_then_scan;\n'
                  ' (void)gb_partition; (void)gb_scan_segmented; (void)gb_scan_then_fan;\n'
-                 ' (void)gb_device_error; (void)gb_last_cuda_error; (void)gb_set_profile_events;\n'
+                 ' (void)gb_device_error; (void)gb_last_device_error; (void)gb_last_cuda_error;\n'
+                 ' (void)gb_set_profile_events;\n'
                  ' (void)gb_set_wait_limit_ns; (void)gb_set_stalled_tile;\n'
                  ' return t > 0 && gb_version() > 0 ? 0 : 1; }\n')
     exe = tmp_path / "use"
@@ -121,6 +123,15 @@ def test_argument_checks_before_cuda(lib):
     assert lib.gb_scan_segmented(gb.F32, gb.MAX, 0, p, p, p, 10, None, None, 0, None) == gb.ERR_NO_IDENTITY
     assert lib.gb_scan_segmented(gb.F32, gb.ADD, 1, p, None, p, 10, None, None, 0, None) == gb.ERR_INVALID
     assert lib.gb_scan_segmented(gb.F32, gb.ADD, 1, p, p, p, 0, None, None, 0, None) == gb.OK
+    # the no-allocation scan: the same checks as gb_scan_inclusive, before any CUDA call
+    assert lib.gb_scan_inclusive_noalloc(gb.F32, gb.ADD, p, p, -1, None) == gb.ERR_INVALID
+    assert lib.gb_scan_inclusive_noalloc(9, gb.ADD, p, p, 0, None) == gb.ERR_INVALID
+    assert lib.gb_scan_inclusive_noalloc(gb.F32, 5, p, p, 0, None) == gb.ERR_INVALID
+    assert lib.gb_scan_inclusive_noalloc(gb.F32, gb.ADD, p, p, 0, None) == gb.OK
+    assert lib.gb_scan_inclusive_noalloc(gb.F32, gb.ADD, p, p, 1 << 40, None) == gb.ERR_RANGE
+    # the per-call status needs the call's scratch (256-byte aligned)
+    assert lib.gb_last_device_error(None, None) == gb.ERR_INVALID
+    assert lib.gb_last_device_error(ctypes.c_void_p(258), None) == gb.ERR_INVALID
 
 
 def test_valid_call_without_gpu_fails_loudly(lib):
