@@ -275,15 +275,16 @@ __device__ __forceinline__ void pdl_entry() {
 
 // ---- warp scan -------------------------------------------------------------------
 
-// Register-only inclusive warp scan: five __shfl_up_sync doubling steps, each add
-// guarded by the lane index so the low lanes keep their own value (The CUDA
-// Handbook, 13.3.1, Listing 13-4).  The guard needs no identity element, so the
-// same code serves MAX / MIN.
+// Inclusive scan over the 32 lanes of a warp, in registers (The CUDA Handbook,
+// 13.3.1).  In the step of distance d each lane takes the running value of the lane d
+// below it and combines it on its left; after the step a lane covers the 2d lanes
+// ending at it.  Lanes below d have nothing below them and keep their value, which is
+// what lets operators without a neutral element (MAX, MIN) use it unchanged.
 template <class T, int OP> __device__ __forceinline__ T warp_inclusive(T v, int lane) {
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    T n = __shfl_up_sync(0xffffffffu, v, off);
-    if (lane >= off) v = Op<T, OP>::f(n, v);
+  for (int d = 1; d < 32; d *= 2) {
+    const T below = __shfl_up_sync(0xffffffffu, v, d);
+    v = lane >= d ? Op<T, OP>::f(below, v) : v;
   }
   return v;
 }

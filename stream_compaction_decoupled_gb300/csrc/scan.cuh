@@ -2,12 +2,15 @@
 // array.  C == 1 (contiguous rows): one row, or a few long rows, that fit in L2 go
 // to the segment kernel (fp64: its thread-contiguous variant, one row), one row many
 // times larger than L2 to the L2-resident look-back kernel, everything else to the
-// row kernel.  C > 1 (lanes / columns): the lane look-back kernel, or for 8-byte lanes
-// in a few long chains that fit in L2, reduce-then-scan.
+// row kernel.  C > 1 (lanes / columns): one aligned chain of 4, 8 or 16 four-byte
+// lanes that fits in L2 goes to the lane segment kernel, 8-byte lanes in a few long
+// chains that fit in L2 to reduce-then-scan, everything else to the lane look-back
+// kernel.
 #pragma once
 
 #include "scan_lanes.cuh"
 #include "scan_lanes_rts.cuh"
+#include "scan_lanes_seg.cuh"
 #include "scan_rows.cuh"
 #include "scan_seg.cuh"
 #include "scan_stash.cuh"
@@ -24,7 +27,14 @@ template <class T> size_t scan_temp_bytes(long long B, long long R, long long C)
     return m > seg ? m : seg;
   }
   if (lanes_rts_applies<T>(B, R, C)) return lanes_rts_temp_bytes<T>(B, R, C);
-  return lanes_temp_bytes<T>(B, R, C);
+  const size_t lt = lanes_temp_bytes<T>(B, R, C);
+  if constexpr (sizeof(T) == 4) {
+    if (B == 1 && (C == 4 || C == 8 || C == 16)) {  // the lane segment kernel may run
+      const size_t st = lanes_seg_temp_bytes<T>();
+      return lt > st ? lt : st;
+    }
+  }
+  return lt;
 }
 
 template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& ctx) {
@@ -66,6 +76,16 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
       case OP_MAX: return launch_rows_op<T, OP_MAX>(job, ctx);
       case OP_MUL: return launch_rows_op<T, OP_MUL>(job, ctx);
       default: return launch_rows_op<T, OP_MIN>(job, ctx);
+    }
+  }
+  if constexpr (sizeof(T) == 4) {
+    if (lanes_seg_applies<T>(job)) {
+      switch (job.op) {
+        case OP_ADD: return launch_lanes_seg_op<T, OP_ADD>(job, ctx);
+        case OP_MAX: return launch_lanes_seg_op<T, OP_MAX>(job, ctx);
+        case OP_MUL: return launch_lanes_seg_op<T, OP_MUL>(job, ctx);
+        default: return launch_lanes_seg_op<T, OP_MIN>(job, ctx);
+      }
     }
   }
   if constexpr (sizeof(T) == 8) {
