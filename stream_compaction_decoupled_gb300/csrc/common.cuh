@@ -149,6 +149,17 @@ template <class T> __device__ __forceinline__ void st_relaxed(T* p, T v) {
   else st_relaxed_u32((unsigned*)p, to_u32(v));
 }
 
+// Acquire / release on a shared-memory flag within the CTA (one warp posts values in
+// shared memory, the others read them once they see the flag).
+__device__ __forceinline__ unsigned ld_acquire_cta_shared(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"((unsigned)__cvta_generic_to_shared(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta_shared(unsigned* p, unsigned v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"((unsigned)__cvta_generic_to_shared(p)), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

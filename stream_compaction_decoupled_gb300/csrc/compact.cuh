@@ -254,16 +254,6 @@ template <class T> struct CompactSegArgs : SegArgsBase {
 
 constexpr int kCompactStageCap = 1536;  // indices a warp can stage before the base is known
 
-// Acquire / release on a shared-memory flag within the CTA.
-__device__ __forceinline__ unsigned ld_acquire_cta_shared(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_cta_shared(unsigned* p, unsigned v) {
-  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-
 template <class T, int PRED, class G>
 __global__ void __launch_bounds__(G::NT, G::MINB) compact_seg_kernel(CompactSegArgs<T> a, PackedStatus<unsigned> st) {
   pdl_entry();
