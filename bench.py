@@ -76,6 +76,9 @@ KERNEL_SOURCES = {
     "lanes_rts_reduce_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
     "lanes_rts_spine_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
     "lanes_rts_scan_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_lanes.cuh", "scan_lanes_rts.cuh"),
+    "scan_lanes_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "scan_lanes_seg.cuh"),
+    "scan_affine_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "scan_affine.cuh"),
+    "scan_affine_tile_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "scan_affine.cuh"),
 }
 
 
@@ -368,6 +371,82 @@ def secondary_workloads(device, hbm_peak, reps=10, only=None):
     return out
 
 
+# ------------------------------------------------------------ FP64 add rate ---
+
+# A throughput probe of the FP64 adder (the bound of the fp64 scans on GB300), written
+# out, built with nvcc and run by --fp64-add-rate.  Every thread runs 8 independent
+# chains of dependent adds (one add per chain per iteration), so the adder, not the
+# latency of one chain, is the limit; 8 CTAs of 256 threads per SM.  The result is
+# written to memory so the adds are not removed.
+_ADD_RATE_SRC = r"""
+#include <cstdio>
+template <class T> __global__ void chains(T* out, T step, int iters) {
+  T c[8];
+  for (int k = 0; k < 8; ++k) c[k] = (T)(threadIdx.x + k);
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) c[k] += step;
+  }
+  T s = 0;
+  for (int k = 0; k < 8; ++k) s += c[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+template <class T> void rate(const char* name) {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
+  const int blocks = sms * 8, threads = 256, iters = 4096;
+  T* out = nullptr;
+  cudaMalloc(&out, sizeof(T) * blocks * threads);
+  cudaEvent_t a, b;
+  cudaEventCreate(&a);
+  cudaEventCreate(&b);
+  float best = 1e30f;
+  for (int r = 0; r < 7; ++r) {
+    cudaEventRecord(a);
+    chains<T><<<blocks, threads>>>(out, (T)1e-9, iters);
+    cudaEventRecord(b);
+    cudaEventSynchronize(b);
+    float ms = 0;
+    cudaEventElapsedTime(&ms, a, b);
+    if (ms < best) best = ms;
+  }
+  const double adds = (double)blocks * threads * iters * 8;
+  printf("%s %d %.6f %.1f %s\n", name, sms, best, adds, cudaGetErrorString(cudaGetLastError()));
+  cudaFree(out);
+}
+int main() {
+  rate<double>("fp64");
+  rate<float>("fp32");
+  return 0;
+}
+"""
+
+
+def fp64_add_rate() -> dict:
+    """Build and run the add-rate probe: adds per second and per clock per SM for
+    fp64 and fp32 (best of 7 launches, CUDA events)."""
+    import tempfile
+    nvcc = os.environ.get("NVCC") or "/usr/local/cuda/bin/nvcc"
+    with tempfile.TemporaryDirectory() as tmp:
+        src, exe = os.path.join(tmp, "add_rate.cu"), os.path.join(tmp, "add_rate")
+        with open(src, "w") as f:
+            f.write(_ADD_RATE_SRC)
+        subprocess.run([nvcc, "-O3", "-gencode", "arch=compute_103a,code=sm_103a", src, "-o", exe], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+    peaks = {}
+    if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")):
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    mhz = peaks.get("sm_max_mhz", 2070.0)
+    res = {"sm_clock_mhz_assumed": mhz}
+    for line in out.splitlines():
+        name, sms, ms, adds, err = line.split(maxsplit=4)
+        rate = float(adds) / (float(ms) * 1e-3)
+        res[name] = {"adds_per_s": rate, "per_clock_per_sm": rate / (int(sms) * mhz * 1e6), "ms": float(ms),
+                     "status": err}
+    return res
+
+
 # ---------------------------------------------------------------- CPU oracle ---
 
 def host_cpu() -> dict:
@@ -591,7 +670,13 @@ def our_arm(args, rank, world, local_rank):
         c = extra.get("compact_p0.5")
         if c:
             line["compaction_headline"] = {"workload": "compact_p0.5 (fp32 1e7, x<0.5)",
-                                           "value": c["throughput"], "unit": "Gelem/s"}
+                                           "value": c["throughput"], "unit": "Gelem/s",
+                                           "by_selectivity": {
+                                               k.split("_p")[1]: {"Gelem_s": extra[k]["throughput"],
+                                                                  "kernel_us": extra[k]["kernel_us_best"],
+                                                                  "frac_hbm": extra[k]["frac_hbm"]}
+                                               for k in ("compact_p0.01", "compact_p0.5", "compact_p0.99")
+                                               if k in extra}}
     print(json.dumps(line), flush=True)
 
 
@@ -609,9 +694,14 @@ def main(argv=None):
                     help="headline size (default 1e8); smaller values are for profiling runs only")
     ap.add_argument("--profile", metavar="WORKLOAD", default=None,
                     help="run only WORKLOAD's call (3 untimed, then --steps with L2 flushed) for ncu")
+    ap.add_argument("--fp64-add-rate", action="store_true",
+                    help="build and run the FP64 / FP32 add-rate probe (the fp64 scans' roofline), print it, exit")
     ap.add_argument("--source-hash", metavar="KERNEL", default=None,
                     help="print the source hash that profiles/ summaries of KERNEL record, and exit")
     args = ap.parse_args(argv)
+    if args.fp64_add_rate:
+        print(json.dumps(fp64_add_rate()))
+        return
     if args.source_hash:
         print(kernel_source_hash(args.source_hash))
         return

@@ -168,6 +168,9 @@ WORKLOADS = [
              extra={"p_head": 0.001, "flag_seed": 23}),
     # Stable partition (x < 0.5 first) of the compaction input's shape, values and indices.
     Workload("partition_p0.5", "partition", "float32", (10_000_000,), "uniform01", 21, extra={"p": 0.5}),
+    # An operator that is not commutative: 1e7 affine maps (a, b) of int32 under
+    # composition (the first-order recurrence y_i = a_i y_{i-1} + b_i), 80 MB each way.
+    Workload("i32_1e7_affine", "scan", "int32", (10_000_000,), "ints", 24, op="affine", lanes=2),
 ]
 
 BY_NAME = {w.name: w for w in WORKLOADS}

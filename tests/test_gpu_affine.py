@@ -153,3 +153,15 @@ def test_affine_argument_errors():
     assert lib.gb_scan_then_fan(gb.I32, gb.AFFINE, 1, p, p, 16, None, None, 0, s) == gb.ERR_UNSUPPORTED
     assert lib.gb_scan_inclusive(gb.I32, 2, gb.AFFINE, p, p, 0, None, 0, s) == gb.OK
     assert gb.device_error() == gb.OK
+
+
+def test_affine_full_size_workload():
+    """The benchmark's i32_1e7_affine workload, bit for bit, inclusive and exclusive."""
+    w = workloads.BY_NAME["i32_1e7_affine"]
+    x = w.make()
+    xd, out = on_device(x, 0)
+    gb.scan_inclusive(xd, "affine", lanes=2, out=out)
+    check(out, x, True, None, "i32_1e7_affine incl")
+    gb.scan_exclusive(xd, "affine", lanes=2, out=out)
+    check(out, x, False, None, "i32_1e7_affine excl")
+    assert gb.device_error() == gb.OK
