@@ -85,7 +85,7 @@ def test_fuzz_scan(case):
     inclusive = bool(r.random() < 0.5)
     lanes = 1
     if r.random() < 0.25:
-        lanes = int(r.choice([2, 3, 8, 24] + ([17] if dt == "f64" else [])))
+        lanes = int(r.choice([2, 3, 4, 8, 16, 24] + ([17] if dt == "f64" else [])))
     n = draw_n(r, MAX_VALUES // lanes)
     off = 0 if r.random() < 0.6 else int(r.integers(1, 4))
     x = scan_values(dt, op, n * lanes + off, 7_000 + case)
@@ -275,4 +275,36 @@ def test_fuzz_host_scan(case):
     out = gb.scan_inclusive_host(xh, op, chunk_elems=chunk)
     torch.cuda.current_stream().synchronize()
     assert_scan_matches(out.numpy(), as3(x, 1, n, 1), op, True, what=what)
+    assert gb.device_error() == gb.OK, what
+
+
+@pytest.mark.parametrize("case", range(120))
+def test_fuzz_affine(case):
+    """Composition of affine maps (two lanes of an integer type): sizes around the
+    segment kernel's chunks and past the point where every warp has one, views 0 to 3
+    maps off alignment (32-bit maps are 8 bytes: odd offsets take the look-back tile
+    kernel), inclusive and exclusive with and without an initial map; bit for bit."""
+    r = np.random.default_rng(15_000 + case)
+    dt = str(r.choice(["i32", "u32", "i64", "u64"]))
+    npt = NP[dt]
+    n = draw_n(r, 2_000_000)
+    off = 0 if r.random() < 0.5 else int(r.integers(1, 4))
+    inclusive = bool(r.random() < 0.5)
+    bits = 8 * np.dtype(npt).itemsize
+    init = None
+    if not inclusive and r.random() < 0.6:  # a full-range initial map (a, b)
+        init = workloads.full_range_uints(2, 16_000 + case, np.uint32 if bits == 32 else np.uint64).view(npt)
+    x = workloads.full_range_uints(2 * (n + off), 15_000 + case, np.uint32 if bits == 32 else np.uint64)
+    x = x.view(npt) if np.dtype(npt).kind == "i" else x
+    xv = x[2 * off:]
+    xd = dev(x)[2 * off:]
+    what = "case %d: %s n=%d off=%d %s init=%r" % (case, dt, n, off, "incl" if inclusive else "excl", init)
+    got = (gb.scan_inclusive(xd, "affine", lanes=2) if inclusive
+           else gb.scan_exclusive(xd, "affine", init=init, lanes=2)).cpu().numpy()
+    want = oracle.scan_affine(xv, inclusive, init)
+    ok = got == want
+    if not ok.all():
+        i = int(np.flatnonzero(~ok)[0])
+        raise AssertionError("%s: %d values differ, first at map %d: got %s want %s" % (
+            what, int((~ok).sum()), i // 2, got[i // 2 * 2: i // 2 * 2 + 2], want[i // 2 * 2: i // 2 * 2 + 2]))
     assert gb.device_error() == gb.OK, what
