@@ -190,21 +190,15 @@ using PackGeom = RowsCfg<unsigned, 128, 2, 2, 12>;
 // 2^31, which is the saturating add of the counts), phase 2 publishes the segment
 // sum and gathers the earlier ones, phase 3 walks the warp's chunks again from L2:
 // the exclusive offsets of a chunk (saturating, seeded with the running base) are
-// written out and kept in shared memory, and the chunk's records are emitted in
-// blocks of 32 x PV output slots: lane l takes PV consecutive slots, finds the object
-// owning the first by a binary search over the kept offsets and walks forward (an
-// object without records shares its successor's offset and is stepped over), writes
-// the owners to a per-warp staging buffer (lane l's slot v at l*PV + (v ^ ((l/4) mod
-// PV)): the lanes' writes and the block's reads both hit 32 different banks), and the
-// warp stores the block contiguously.  Measured on GB300 for 1e6 Poisson(4) counts:
-// 20.6 us (8 slots a lane; 16 give 20.9 us) against 42.8 us for the tile kernel.
+// written out, and the chunk's records are emitted in blocks of 32 x PV output slots
+// by a scatter of the run starts and a forward max over the block (no search; see
+// the emission below), and the warp stores each block contiguously.
 constexpr int PV = 8;
-constexpr int PSW = 2;  // log2(32 / PV): lanes l and l + 32/PV share a bank row
 // Chunks of 128 counts (one 16-byte vector a lane): about 512 records each for the
 // Poisson(4) workload, so that a million counts give every warp of every SM chunks
 // to emit (emission is instruction-bound, not memory-bound).
 using PackSegGeom = SegCfg<unsigned, 1024, 1, 1>;
-constexpr size_t kPackSegSmem = (size_t)PackSegGeom::NW * (PackSegGeom::CH + 32 * PV) * sizeof(unsigned);
+constexpr size_t kPackSegSmem = (size_t)PackSegGeom::NW * 32 * PV * sizeof(unsigned);
 
 struct PackSegArgs : SegArgsBase {
   const int* counts;
@@ -225,8 +219,7 @@ __global__ void __launch_bounds__(PackSegGeom::NT, PackSegGeom::MINB) pack_seg_k
   __shared__ unsigned s_warp[NW];
   __shared__ unsigned s_base;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  unsigned* s_off = pack_seg_smem + warp * (CH + 32 * PV);  // the chunk's offsets
-  unsigned* s_stage = s_off + CH;                            // one block of owners
+  unsigned* s_stage = pack_seg_smem + warp * 32 * PV;  // one block of record slots
   if (tid == 0) s_seg = atomicAdd(a.counter, 1u);
   __syncthreads();
   const unsigned seg = s_seg;
@@ -310,13 +303,14 @@ __global__ void __launch_bounds__(PackSegGeom::NT, PackSegGeom::MINB) pack_seg_k
           x[j].v[e] = 0;
           negative = true;
         }
+    static_assert(ROUNDS == 1, "a lane holds one vector of counts per chunk");
+    const Vec<unsigned> cnt = x[0];  // the (clamped) counts, kept for the emission
     unsigned pre[ROUNDS];
     const unsigned ctot = regs_reduce_pass<unsigned, OP_SATADD, ROUNDS>(x, lane, pre);
     regs_apply_pass<unsigned, OP_SATADD, ROUNDS>(x, lane, pre, run, true, false);  // x: exclusive offsets
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < ROUNDS; ++j) {
-      st_vec<unsigned>(reinterpret_cast<uint4*>(s_off) + j * 32 + lane, x[j]);
       if (a.offsets) {
         const long long e0 = c * CH + (long long)(j * 32 + lane) * VEC;
         Vec<unsigned> o;
@@ -339,31 +333,46 @@ __global__ void __launch_bounds__(PackSegGeom::NT, PackSegGeom::MINB) pack_seg_k
     const unsigned cend_u = Op<unsigned, OP_SATADD>::f(run, ctot);
     const unsigned cb = run, ce = (long long)cend_u < a.capacity ? cend_u : (unsigned)a.capacity;
     const unsigned obj0 = (unsigned)(c * CH);
+    // Records in blocks of 32 x PV slots, with no search: the block's slots are
+    // cleared in shared memory, every object whose run starts in the block writes its
+    // (chunk-local index + 1) at its first slot (distinct objects with records have
+    // distinct offsets), and a forward max over the block fills each slot with its
+    // owner (owners increase with the offset): lane l takes slots PV l .. PV l + PV - 1
+    // serially, one warp max-scan joins the lanes, and `owner` carries the last slot's
+    // owner into the next block.  The warp then stores the block contiguously.
+    static_assert(PV == 8, "two 16-byte vectors of slots a lane");
+    uint4* blk4 = reinterpret_cast<uint4*>(s_stage);
+    unsigned owner = 0;
     for (unsigned b0 = cb; b0 < ce; b0 += 32 * PV) {
-      const unsigned s0 = b0 + (unsigned)lane * PV;
-      if (s0 < ce) {
-        int lo = 0, hi = CH;  // the last object with offset <= s0
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (s_off[mid] <= s0) lo = mid;
-          else hi = mid;
-        }
-        int obj = lo;
+      blk4[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+      blk4[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
+      __syncwarp();
 #pragma unroll
-        for (int v = 0; v < PV; ++v) {
-          const unsigned sl = s0 + v;
-          while (obj + 1 < CH && s_off[obj + 1] <= sl) ++obj;
-          s_stage[lane * PV + (v ^ ((lane >> PSW) & (PV - 1)))] = obj0 + obj;
-        }
+      for (int e = 0; e < VEC; ++e) {
+        const unsigned o = x[0].v[e];
+        if (cnt.v[e] != 0 && o >= b0 && o - b0 < 32u * PV) s_stage[o - b0] = (unsigned)(lane * VEC + e) + 1u;
       }
+      __syncwarp();
+      const uint4 lo = blk4[2 * lane], hi = blk4[2 * lane + 1];
+      unsigned v[PV] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+      for (int i = 1; i < PV; ++i) v[i] = max(v[i], v[i - 1]);
+      const unsigned inc = warp_inclusive<unsigned, OP_MAX>(v[PV - 1], lane);
+      unsigned before = __shfl_up_sync(0xffffffffu, inc, 1);
+      before = max(lane > 0 ? before : 0u, owner);
+#pragma unroll
+      for (int i = 0; i < PV; ++i) v[i] = max(v[i], before);
+      owner = max(__shfl_sync(0xffffffffu, inc, 31), owner);
+      __syncwarp();
+      blk4[2 * lane] = make_uint4(v[0], v[1], v[2], v[3]);
+      blk4[2 * lane + 1] = make_uint4(v[4], v[5], v[6], v[7]);
       __syncwarp();
       const unsigned nblk = ce - b0 < 32u * PV ? ce - b0 : 32u * PV;
       int* dst = a.records + b0;
 #pragma unroll
       for (int i = 0; i < PV; ++i) {
         const unsigned k = (unsigned)(lane + 32 * i);
-        const unsigned ln = k / PV, v = k % PV;
-        if (k < nblk) dst[k] = (int)s_stage[ln * PV + (v ^ ((ln >> PSW) & (PV - 1)))];
+        if (k < nblk) dst[k] = (int)(obj0 + s_stage[k] - 1u);
       }
       __syncwarp();
     }
