@@ -213,3 +213,31 @@ def test_pack_saturation(aligned):
     assert np.array_equal(offs.cpu().numpy().astype(np.int64), np.minimum(w_offs, 2**31 - 1))
     assert np.array_equal(recs.cpu().numpy()[:1000], w_recs[:1000])
     assert gb.device_error() == gb.ERR_RANGE
+
+
+@pytest.mark.parametrize("shift", [0, 1, 3, 4, 8])
+@pytest.mark.parametrize("cap_frac", [1.0, 0.37])
+def test_pack_record_alignment(shift, cap_frac):
+    """Records written into a view that starts `shift` words into its buffer (32-byte
+    vector stores only where the view allows them), at full capacity and cut short:
+    the records match the oracle and no word outside [0, capacity) of the view is
+    touched."""
+    n = 200_003
+    rng = np.random.default_rng(shift * 7 + int(cap_frac * 10))
+    k = rng.poisson(4.0, n).astype(np.int32)
+    k[rng.integers(0, n, 40)] = rng.integers(250, 2000, 40).astype(np.int32)  # runs over whole blocks
+    k[rng.random(n) < 0.3] = 0
+    total = int(k.astype(np.int64).sum())
+    cap = int(total * cap_frac)
+    guard = -7
+    buf = torch.full((cap + shift + 64,), guard, dtype=torch.int32, device="cuda")
+    recs_view = buf[shift: shift + cap]
+    offs, recs, tot = gb.pack_by_counts(dev(k), cap, out_records=recs_view)
+    w_offs, w_recs, w_total = oracle.pack_by_counts(k, capacity=cap)
+    assert int(tot.item()) == w_total
+    assert np.array_equal(offs.cpu().numpy().astype(np.int64), w_offs)
+    b = buf.cpu().numpy()
+    assert np.array_equal(b[shift: shift + cap], w_recs[:cap])
+    assert (b[:shift] == guard).all() and (b[shift + cap:] == guard).all()
+    assert gb.device_error() == (gb.OK if cap >= total else gb.ERR_RANGE)
+    assert gb.device_error() == gb.OK
