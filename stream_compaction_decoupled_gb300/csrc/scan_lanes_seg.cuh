@@ -7,7 +7,10 @@
 // of an (R, 8) matrix scanned down axis 0) is thousands of tiles long, and the lane
 // kernel's per-lane look-back walks it tile by tile.  Here every segment (CTA) gets
 // the combination of all earlier segments in one gather, as the 1-D segment kernel
-// does.
+// does.  A segment publishes each lane's aggregate in a word of its own that carries
+// its flag, right after phase 1, and the gather is spread over all but one warp of
+// the CTA, so that every earlier word is requested at once and the base is known
+// one memory round trip after the last of them is visible.
 //
 // An element is V = C / 4 vectors of 16 bytes.  A warp reads a chunk as ROUNDS
 // coalesced rounds of 32 vectors (512 bytes, E = 32 / V whole elements); lane l
@@ -40,11 +43,11 @@ template <class T, int C> struct LanesSegArgs : SegArgsBase {  // n: elements (p
   int inclusive;
 };
 
-// Status of a segment: a flag, and its C lane aggregates in a slot of their own,
-// stored before the flag is released.
+// Status of a segment: C words, one per lane, each (flag << 32 | the lane
+// aggregate's bits).  A lane's value and its flag travel in one 64-bit store, so a
+// reader that sees the flag has the value, with no fence between them.
 template <class T, int C> struct LanesSegStatus {
-  unsigned* flag;
-  T* val;  // [segment][lane]
+  unsigned long long* w;  // [segment][lane]
 };
 
 // A lane's 4 values: one 16-byte vector, the lanes 4s .. 4s+3 of one element.
@@ -142,10 +145,15 @@ __global__ void __launch_bounds__(G::NT, G::MINB)
   __shared__ T s_base[C];
   __shared__ T s_init[C];
   __shared__ int s_hbase;
+  constexpr int GG = (NW - 1) * 32 / C;  // phase 2's gathering blocks (warps 1..)
+  __shared__ T s_part[GG][C];            // their folds
+  __shared__ int s_phas[GG];
+  __shared__ int s_tmo;                  // a gatherer's wait ran out
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = lane % V, member = lane / V;
   if (tid == 0) {
     s_seg = atomicAdd(a.counter, 1u);
+    s_tmo = 0;
 #pragma unroll
     for (int c = 0; c < C; ++c) s_init[c] = a.init[c];  // constant indices: no local copy of the parameter
   }
@@ -209,74 +217,106 @@ __global__ void __launch_bounds__(G::NT, G::MINB)
   }
   __syncthreads();
 
-  // Phase 2 (warp 0): scan the warp totals per lane, publish the segment's C
-  // aggregates, gather the earlier segments'.
+  // Phase 2.  Warp 0 combines the warp totals into the segment's C aggregates and
+  // publishes them at once, then scans the warp totals per lane for phase 3.
+  // Meanwhile the other warps wait for the earlier segments' words and fold them:
+  // thread t of warps 1.. takes lane value t mod C of the consecutive block of
+  // segments (t / C) q .. (t / C) q + q - 1, q = ceil(seg / GG), all its words
+  // requested at once and only the missing ones polled again.  Then warp 0 joins the
+  // blocks, lower ones on the left.  Every combination joins adjacent ranges in order
+  // (a product of ranges that are not adjacent can overflow where every prefix
+  // stays in range).
+  constexpr int K = 32 / C;                        // lanes of warp 0 per lane value
+  constexpr int QMAX = (G::MAXSEG + GG - 1) / GG;  // segments a block takes at most
+  static_assert(QMAX <= 32, "pending bits of one word");
   if (warp == 0) {
-    if (lane < C) {
-      T acc = s_w[0][lane];
-      for (int w = 1; w < nact; ++w) {
-        acc = Op<T, OP>::f(acc, s_w[w][lane]);
-        s_w[w][lane] = acc;
-      }
-      if ((long long)seg != a.stalled) st_relaxed(st.val + (size_t)seg * C + lane, acc);
-      __threadfence();  // the values before the flag
-    }
-    __syncwarp();
-    if (lane == 0 && (long long)seg != a.stalled) st_release_u32(st.flag + seg, FLAG_A);
-    // Wait until every earlier segment has published (lane l watches the flags of
-    // segments l P .. l P + P - 1, P = ceil(seg / 32)), then lane (c, g) = (l mod C,
-    // l / C) combines lane value c of the consecutive block of segments g Q .. g Q +
-    // Q - 1 (Q = ceil(seg / (32 / C))) in order, and the groups combine with the
-    // lower block on the left: only adjacent ranges are ever combined (a product of
-    // ranges that are not adjacent can overflow where every prefix stays in range).
-    bool timed_out = false;
+    const int c = lane % C, k = lane / C;
     T acc{};
-    bool have = false;
-    if (seg > 0) {
-      const unsigned per = (seg + 31) / 32, mine = (unsigned)lane * per;
+    bool h = false;
+    for (int w = k * nact / K; w < (k + 1) * nact / K; ++w) {
+      const T x = s_w[w][c];
+      acc = h ? Op<T, OP>::f(acc, x) : x;
+      h = true;
+    }
+#pragma unroll
+    for (int d = C; d < 32; d *= 2) {  // across k, the lower warps on the left
+      const T o = __shfl_xor_sync(0xffffffffu, acc, d);
+      const bool oh = __shfl_xor_sync(0xffffffffu, (int)h, d) != 0;
+      if (oh) acc = h ? ((lane & d) ? Op<T, OP>::f(o, acc) : Op<T, OP>::f(acc, o)) : o;
+      h = h || oh;
+    }
+    if (k == 0 && (long long)seg != a.stalled)
+      st_relaxed_u64(st.w + (size_t)seg * C + c, ((unsigned long long)FLAG_A << 32) | to_u32(acc));
+    __syncwarp();  // every lane's reads of s_w before the scan rewrites it
+    if (lane < C) {
+      T run = s_w[0][lane];
+      for (int w = 1; w < nact; ++w) {
+        run = Op<T, OP>::f(run, s_w[w][lane]);
+        s_w[w][lane] = run;
+      }
+    }
+  } else {
+    const int t = tid - 32, c = t % C, g = t / C;
+    const unsigned q = (seg + GG - 1) / GG, s0 = (unsigned)g * q, s1 = s0 + q < seg ? s0 + q : seg;
+    if (s0 < s1) {
+      unsigned long long wv[QMAX];
       unsigned pending = 0;
 #pragma unroll
-      for (int k = 0; k < G::M; ++k)
-        if ((unsigned)k < per && mine + k < seg) pending |= 1u << k;
+      for (int j = 0; j < QMAX; ++j)
+        if (s0 + j < s1) pending |= 1u << j;
       unsigned long long t0 = 0;
       for (int spins = 0;; ++spins) {
 #pragma unroll
-        for (int k = 0; k < G::M; ++k)
-          if ((pending & (1u << k)) && ld_acquire_u32(st.flag + mine + k) != FLAG_X) pending &= ~(1u << k);
-        if (__all_sync(0xffffffffu, pending == 0)) break;
-        unsigned long long now = 0;
-        if (lane == 0) now = globaltimer();
-        now = __shfl_sync(0xffffffffu, now, 0);
+        for (int j = 0; j < QMAX; ++j)
+          if (pending & (1u << j)) {
+            wv[j] = ld_relaxed_u64(st.w + (size_t)(s0 + j) * C + c);
+            if ((unsigned)(wv[j] >> 32) != FLAG_X) pending &= ~(1u << j);
+          }
+        if (pending == 0) break;
+        const unsigned long long now = globaltimer();
         if (spins == 0) t0 = now;
-        else if (now - t0 > a.wait_ns) {
-          timed_out = true;
+        else if (now - t0 > a.wait_ns) {  // the words still missing are left out
+          s_tmo = 1;
           break;
         }
         backoff(spins);
       }
-      __syncwarp();
-      // Segments whose flags this warp saw set carry their values; after a time-out
-      // the values of the others are read as they stand (the call reports the error).
-      __threadfence();  // every lane's acquire above orders the value reads below
-      const int c = lane % C, g = lane / C;
-      constexpr int GS = 32 / C;  // groups
-      const unsigned q = (seg + GS - 1) / GS, s1 = (g + 1) * q < seg ? (g + 1) * q : seg;
-      for (unsigned sg = (unsigned)g * q; sg < s1; ++sg) {
-        const T x = ld_relaxed(st.val + (size_t)sg * C + c);
+      T acc{};
+      bool h = false;
+#pragma unroll
+      for (int j = 0; j < QMAX; ++j)
+        if (s0 + j < s1 && !(pending & (1u << j))) {
+          const T x = from_u32<T>((unsigned)wv[j]);
+          acc = h ? Op<T, OP>::f(acc, x) : x;
+          h = true;
+        }
+      s_part[g][c] = acc;
+      if (c == 0) s_phas[g] = h;
+    } else if (c == 0) {
+      s_phas[g] = 0;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int c = lane % C, k = lane / C;
+    T acc{};
+    bool have = false;
+    for (int g = k * GG / K; g < (k + 1) * GG / K; ++g)
+      if (s_phas[g]) {
+        const T x = s_part[g][c];
         acc = have ? Op<T, OP>::f(acc, x) : x;
         have = true;
       }
 #pragma unroll
-      for (int d = C; d < 32; d *= 2) {  // across the groups, the lower one on the left
-        const T o = __shfl_xor_sync(0xffffffffu, acc, d);
-        const bool oh = __shfl_xor_sync(0xffffffffu, (int)have, d) != 0;
-        if (oh) acc = have ? ((lane & d) ? Op<T, OP>::f(o, acc) : Op<T, OP>::f(acc, o)) : o;
-        have = have || oh;
-      }
+    for (int d = C; d < 32; d *= 2) {  // across the blocks of k, the lower ones on the left
+      const T o = __shfl_xor_sync(0xffffffffu, acc, d);
+      const bool oh = __shfl_xor_sync(0xffffffffu, (int)have, d) != 0;
+      if (oh) acc = have ? ((lane & d) ? Op<T, OP>::f(o, acc) : Op<T, OP>::f(acc, o)) : o;
+      have = have || oh;
     }
     if (lane < C) s_base[lane] = acc;
     if (lane == 0) {
-      if (timed_out) raise_err(a.err, ERRBIT_TIMEOUT);
+      if (s_tmo) raise_err(a.err, ERRBIT_TIMEOUT);
       s_hbase = have;
     }
   }
@@ -353,7 +393,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB)
 
 template <class T, int V> size_t lanes_seg_status_bytes() {
   using G = LanesSegCfg<T, V>;
-  return round_up((size_t)G::MAXSEG * 4, 256) + round_up((size_t)G::MAXSEG * G::C * sizeof(T), 256);
+  return round_up((size_t)G::MAXSEG * G::C * 8, 256);
 }
 // Scratch for any lane count this kernel serves (the largest, 16 lanes).
 template <class T> size_t lanes_seg_temp_bytes() { return kHeaderBytes + lanes_seg_status_bytes<T, 4>(); }
@@ -388,11 +428,9 @@ template <class T, int OP, int V> cudaError_t launch_lanes_seg_v(const ScanJob& 
   }
   a.inclusive = job.inclusive;
   LanesSegStatus<T, G::C> st;
-  char* base = (char*)job.temp + kHeaderBytes;
-  st.flag = (unsigned*)base;
-  st.val = (T*)(base + round_up((size_t)G::MAXSEG * 4, 256));
+  st.w = (unsigned long long*)((char*)job.temp + kHeaderBytes);
   profile_before(ctx);
-  cudaError_t e = clear_status(job.temp, kHeaderBytes + (size_t)G::MAXSEG * 4, nullptr, 0, ctx);
+  cudaError_t e = clear_status(job.temp, kHeaderBytes + (size_t)p.ctas * G::C * 8, nullptr, 0, ctx);
   if (e == cudaSuccess) e = launch_pdl(scan_lanes_seg_kernel<T, OP, G>, p.ctas, G::NT, 0, ctx.stream, a, st);
   profile_after(ctx);
   return e;
