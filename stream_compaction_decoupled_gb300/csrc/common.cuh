@@ -260,6 +260,17 @@ __device__ __forceinline__ uint4 ld_hint(const uint4* p, unsigned long long pol)
                : "l"(p), "l"(pol));
   return r;
 }
+// The same load allocating in L1: for layouts in which each lane owns 64 consecutive
+// bytes, so that one instruction reads 16 bytes of each of 32 sectors 64 bytes apart
+// and the next three read the rest of the same sectors.  Without L1 allocation each
+// sector would travel from L2 twice.
+__device__ __forceinline__ uint4 ld_hint_l1(const uint4* p, unsigned long long pol) {
+  uint4 r;
+  asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
 __device__ __forceinline__ void st_hint(uint4* p, uint4 v, unsigned long long pol) {
   asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w), "l"(pol)

@@ -93,7 +93,7 @@ __device__ __forceinline__ void aff_load(Aff<T> (&x)[K], const T* in, long long 
     const uint4* p = reinterpret_cast<const uint4*>(in + 2 * e0);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint4 u = ld_hint(p + q, pol);
+      const uint4 u = ld_hint_l1(p + q, pol);
       memcpy(reinterpret_cast<char*>(x) + 16 * q, &u, 16);
     }
   } else {
@@ -186,6 +186,37 @@ template <class T> struct AffStatus {
   }
 };
 
+// The segment kernel's status (aggregates only): every 8-byte piece of a segment's
+// map and its complement, in relaxed stores; a reader takes the map once each piece
+// has its complement beside it (the words start at zero each launch, so an accepted
+// pair always holds the piece written).  No flag is released after the values, so a
+// gather needs no acquire and keeps all its loads in flight together.
+template <class T> struct AffSegStatus {
+  static constexpr int P = sizeof(Aff<T>) / 8;  // 8-byte pieces of a map
+  unsigned long long* w;                        // [segment][P][2]
+  __device__ __forceinline__ void publish(long long i, const Aff<T>& v) const {
+    unsigned long long x[P];
+    memcpy(x, &v, sizeof(x));
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      st_relaxed_u64(w + (i * P + j) * 2, x[j]);
+      st_relaxed_u64(w + (i * P + j) * 2 + 1, ~x[j]);
+    }
+  }
+  __device__ __forceinline__ bool poll(long long i, Aff<T>& v) const {
+    unsigned long long x[P];
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      x[j] = ld_relaxed_u64(w + (i * P + j) * 2);
+      ok = ok && ld_relaxed_u64(w + (i * P + j) * 2 + 1) == ~x[j];
+    }
+    memcpy(&v, x, sizeof(x));
+    return ok;
+  }
+};
+static_assert(sizeof(Aff<unsigned>) == 8 && sizeof(Aff<unsigned long long>) == 16, "maps are whole 8-byte pieces");
+
 template <class T> size_t aff_status_bytes(size_t units) {
   return round_up(units * 4, 256) + 2 * round_up(units * sizeof(Aff<T>), 256);
 }
@@ -223,7 +254,7 @@ template <class T> struct AffSegCfg {
 // for (bounded by wait_ns).  Lane l takes the consecutive block [l P, l P + P), P =
 // ceil(cnt / 32); blocks then combine in lane order.  Returns it in every lane.
 template <class T, int M>
-__device__ __forceinline__ Aff<T> aff_gather(const AffStatus<T>& st, unsigned cnt, unsigned long long wait_ns,
+__device__ __forceinline__ Aff<T> aff_gather(const AffSegStatus<T>& st, unsigned cnt, unsigned long long wait_ns,
                                              bool& timed_out) {
   const int lane = threadIdx.x & 31;
   const unsigned per = (cnt + 31) / 32, mine = (unsigned)lane * per;
@@ -240,9 +271,9 @@ __device__ __forceinline__ Aff<T> aff_gather(const AffStatus<T>& st, unsigned cn
 #pragma unroll
     for (int k = 0; k < M; ++k)
       if (pending & (1u << k)) {
-        const unsigned f = st.poll(mine + k);
-        if (f != FLAG_X) {
-          val[k] = st.fetch(mine + k, f);
+        Aff<T> v;
+        if (st.poll(mine + k, v)) {
+          val[k] = v;
           pending &= ~(1u << k);
         }
       }
@@ -265,7 +296,7 @@ __device__ __forceinline__ Aff<T> aff_gather(const AffStatus<T>& st, unsigned cn
 }
 
 template <class T, class G>
-__global__ void __launch_bounds__(G::NT, G::MINB) scan_affine_seg_kernel(AffArgs<T> a, AffStatus<T> st) {
+__global__ void __launch_bounds__(G::NT, G::MINB) scan_affine_seg_kernel(AffArgs<T> a, AffSegStatus<T> st) {
   pdl_entry();
   constexpr int NW = G::NW, K = G::K, CH = G::CH;
   __shared__ unsigned s_seg;
@@ -281,15 +312,21 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_affine_seg_kernel(AffArgs
   const int nact = seg_chunks(a, seg, warp, NW, c0, c1);
 
   // Phase 1: the warp's composition of its chunks, in order (evict-last loads, so
-  // the rescan finds the lines in L2).
+  // the rescan finds the lines in L2).  The next chunk is requested before the
+  // current one is folded: with one 2 KB chunk per warp in flight, the SM would wait
+  // on HBM latency instead of moving the input at the bandwidth it shares.
   {
     const unsigned long long keep = l2_policy_evict_last();
     Aff<T> w = aff_identity<T>();
+    Aff<T> x[K];
+    if (c0 < c1) aff_load<T, K>(x, a.in, c0 * CH + (long long)lane * K, a.n, true, keep);
     for (long long c = c0; c < c1; ++c) {
-      Aff<T> x[K];
-      aff_load<T, K>(x, a.in, c * CH + (long long)lane * K, a.n, true, keep);
+      Aff<T> nx[K];
+      if (c + 1 < c1) aff_load<T, K>(nx, a.in, (c + 1) * CH + (long long)lane * K, a.n, true, keep);
       const Aff<T> inc = aff_warp_inclusive(aff_fold<T, K>(x), lane);
       w = aff_then(w, aff_shfl_idx(inc, 31));
+#pragma unroll
+      for (int k = 0; k < K; ++k) x[k] = nx[k];
     }
     if (lane == 0) s_w[warp] = w;
   }
@@ -302,7 +339,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_affine_seg_kernel(AffArgs
     v = aff_warp_inclusive(v, lane);
     if (lane < nact) s_w[lane] = v;
     const Aff<T> agg = aff_shfl_idx(v, 31);
-    if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, FLAG_A, agg);
+    if (lane == 0 && (long long)seg != a.stalled) st.publish(seg, agg);
     Aff<T> before = aff_identity<T>();
     bool timed_out = false;
     if (seg > 0) before = aff_gather<T, G::M>(st, seg, a.wait_ns, timed_out);
@@ -317,10 +354,14 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_affine_seg_kernel(AffArgs
   Aff<T> carry = s_base;
   if (warp > 0) carry = aff_then(carry, s_w[warp - 1]);
   const unsigned long long drop = l2_policy_evict_first();
+  Aff<T> nx[K];  // the next chunk, requested before this one is scanned
+  if (c0 < c1) aff_load<T, K>(nx, a.in, c0 * CH + (long long)lane * K, a.n, true, drop);
   for (long long c = c0; c < c1; ++c) {
     Aff<T> x[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) x[k] = nx[k];
     const long long e0 = c * CH + (long long)lane * K;
-    aff_load<T, K>(x, a.in, e0, a.n, true, drop);
+    if (c + 1 < c1) aff_load<T, K>(nx, a.in, e0 + CH, a.n, true, drop);
     const Aff<T> inc = aff_warp_inclusive(aff_fold<T, K>(x), lane);
     const Aff<T> pre = aff_then(carry, aff_lane_exclusive(inc, lane));
     carry = aff_then(carry, aff_shfl_idx(inc, 31));
@@ -477,9 +518,10 @@ template <class T> cudaError_t launch_affine(const ScanJob& job, const LaunchCtx
     a.nc = p.nc;
     a.segs = p.segs;
     a.ctas = p.ctas;
-    const AffStatus<T> st = aff_status<T>(job.temp, G::MAXSEG);
+    AffSegStatus<T> st;
+    st.w = (unsigned long long*)((char*)job.temp + kHeaderBytes);  // within aff_status_bytes(MAXSEG)
     profile_before(ctx);
-    e = clear_status(job.temp, kHeaderBytes + (size_t)G::MAXSEG * 4, nullptr, 0, ctx);
+    e = clear_status(job.temp, kHeaderBytes + (size_t)p.ctas * 2 * sizeof(Aff<T>), nullptr, 0, ctx);
     if (e == cudaSuccess) e = launch_pdl(scan_affine_seg_kernel<T, G>, p.ctas, G::NT, 0, ctx.stream, a, st);
     profile_after(ctx);
     return e;

@@ -42,7 +42,9 @@ template <class T, int NT_, int ROUNDS_, int MINB_> struct SegCfg {
   static constexpr int NT = NT_, NW = NT_ / 32, ROUNDS = ROUNDS_, MINB = MINB_;
   static constexpr int VEC = Vec<T>::N;
   static constexpr int CH = 32 * ROUNDS * VEC;  // elements per chunk
-  static constexpr int MAXSEG = 512;            // segments (CTAs) per launch at most
+  // Segments (CTAs) per launch at most; 8-byte values keep the gather's loads (two
+  // words a segment) within the registers of a 1024-thread CTA.
+  static constexpr int MAXSEG = sizeof(T) == 8 ? 256 : 512;
   static constexpr int M = MAXSEG / 32;         // earlier aggregates per lane in phase 2
 };
 // 8-byte elements take 2 rounds a chunk (the chunk and the one prefetched behind it
@@ -390,31 +392,67 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_seg_kernel(SegArgs<T> a, 
   }
 }
 
-// Status area: MAXSEG descriptors right after the header.
+// Status area right after the header: descriptors for up to kSegSlots segments (the
+// most any segment-scheme kernel launches), as the flag-carrying layouts of the
+// segmented scans (StatusFor) or as the segment kernels' words (SegStatusFor).
+constexpr int kSegSlots = 512;
 template <class T> size_t seg_status_bytes() {
-  using G = SegGeom<T>;
-  if (sizeof(T) == 4) return round_up((size_t)G::MAXSEG * 8, 256);
-  return round_up((size_t)G::MAXSEG * 4, 256) + 2 * round_up((size_t)G::MAXSEG * sizeof(T), 256);
+  if (sizeof(T) == 4) return round_up((size_t)kSegSlots * 8, 256);
+  return round_up((size_t)kSegSlots * 4, 256) + 2 * round_up((size_t)kSegSlots * sizeof(T), 256);
 }
 template <class T> typename StatusFor<T>::type seg_status(void* temp) {
-  using G = SegGeom<T>;
   typename StatusFor<T>::type st;
   char* base = (char*)temp + kHeaderBytes;
   if constexpr (sizeof(T) == 4) {
     st.w = (unsigned long long*)base;
   } else {
     st.flag = (unsigned*)base;
-    base += round_up((size_t)G::MAXSEG * 4, 256);
+    base += round_up((size_t)kSegSlots * 4, 256);
     st.agg = (T*)base;
-    base += round_up((size_t)G::MAXSEG * sizeof(T), 256);
+    base += round_up((size_t)kSegSlots * sizeof(T), 256);
     st.pfx = (T*)base;
   }
   return st;
 }
 // Bytes to clear before a launch: the header and the flags.
 template <class T> size_t seg_reset_bytes() {
-  using G = SegGeom<T>;
-  return kHeaderBytes + (sizeof(T) == 4 ? (size_t)G::MAXSEG * 8 : (size_t)G::MAXSEG * 4);
+  return kHeaderBytes + (sizeof(T) == 4 ? (size_t)kSegSlots * 8 : (size_t)kSegSlots * 4);
+}
+
+// Status of the segment kernels' aggregates (they publish aggregates only).  4-byte
+// values: the packed (flag, value) word.  8-byte values: the value's bits and their
+// complement in two relaxed stores; a reader loads both, in flight together, and
+// takes the value once one word is the complement of the other.  Both words are
+// zero before the launch, so every pair a reader accepts holds the value written
+// ((v, 0) passes only when v is all ones, (0, ~v) only when v is 0).  Unlike a flag
+// released after the value, this needs no acquire: a gather keeps all its loads in
+// flight at once.
+template <class T> struct WordPairStatus {
+  unsigned long long* w;  // [segment][2]
+  __device__ __forceinline__ void publish(long long i, unsigned, T v) const {
+    const unsigned long long x = to_u64(v);
+    st_relaxed_u64(w + 2 * i, x);
+    st_relaxed_u64(w + 2 * i + 1, ~x);
+  }
+  __device__ __forceinline__ unsigned poll(long long i, T& v) const {
+    const unsigned long long x0 = ld_relaxed_u64(w + 2 * i), x1 = ld_relaxed_u64(w + 2 * i + 1);
+    v = from_u64<T>(x0);
+    return x1 == ~x0 ? FLAG_A : FLAG_X;
+  }
+  __device__ __forceinline__ T fetch(long long, unsigned, T polled) const { return polled; }
+};
+template <class T> struct SegStatusFor {
+  using type = typename std::conditional<sizeof(T) == 4, PackedStatus<T>, WordPairStatus<T>>::type;
+};
+template <class T> typename SegStatusFor<T>::type seg_word_status(void* temp) {
+  typename SegStatusFor<T>::type st;
+  st.w = (unsigned long long*)((char*)temp + kHeaderBytes);
+  return st;
+}
+// Bytes to clear before a launch of `ctas` segments (within seg_status_bytes).
+static_assert(kSegSlots * 16 <= kSegSlots * 4 + 2 * kSegSlots * 8, "word pairs fit the 8-byte status area");
+template <class T> size_t seg_word_reset_bytes(unsigned ctas) {
+  return kHeaderBytes + (size_t)ctas * (sizeof(T) == 4 ? 8 : 16);
 }
 
 // Inputs up to this size go to this kernel.  Measured on GB300 (fp32 add, L2
@@ -460,9 +498,9 @@ cudaError_t launch_seg_op(const ScanJob& job, const LaunchCtx& ctx) {
   a.inclusive = job.inclusive;
   a.carry_in = (const T*)job.carry_in;
   a.carry_out = (T*)job.carry_out;
-  auto st = seg_status<T>(job.temp);
+  auto st = seg_word_status<T>(job.temp);
   profile_before(ctx);
-  cudaError_t e = clear_status(job.temp, seg_reset_bytes<T>(), nullptr, 0, ctx);
+  cudaError_t e = clear_status(job.temp, seg_word_reset_bytes<T>(p.ctas), nullptr, 0, ctx);
   if (e == cudaSuccess) e = launch_pdl(scan_seg_kernel<T, OP, G, decltype(st)>, p.ctas, G::NT, 0, ctx.stream, a, st);
   profile_after(ctx);
   return e;
@@ -513,10 +551,7 @@ __device__ __forceinline__ void lane_load(T (&x)[KH], const T* in, long long e0,
     const uint4* p = reinterpret_cast<const uint4*>(in + e0);
 #pragma unroll
     for (int j = 0; j < KH / VEC; ++j) {
-      uint4 u;
-      asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                   : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
-                   : "l"(p + j), "l"(pol));
+      const uint4 u = ld_hint_l1(p + j, pol);
       memcpy(&x[j * VEC], &u, 16);
     }
   } else {
@@ -720,12 +755,12 @@ cudaError_t launch_seg_chunk_op(const ScanJob& job, const LaunchCtx& ctx) {
   a.inclusive = job.inclusive;
   a.carry_in = (const T*)job.carry_in;
   a.carry_out = (T*)job.carry_out;
-  auto st = seg_status<T>(job.temp);
+  auto st = seg_word_status<T>(job.temp);
   auto kern = scan_seg_chunk_kernel<T, OP, G, decltype(st)>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::SMEM);
   if (e != cudaSuccess) return e;
   profile_before(ctx);
-  e = clear_status(job.temp, seg_reset_bytes<T>(), nullptr, 0, ctx);
+  e = clear_status(job.temp, seg_word_reset_bytes<T>(p.ctas), nullptr, 0, ctx);
   if (e == cudaSuccess) e = launch_pdl(kern, p.ctas, G::NT, G::SMEM, ctx.stream, a, st);
   profile_after(ctx);
   return e;

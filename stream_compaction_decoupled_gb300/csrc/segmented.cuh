@@ -72,7 +72,7 @@ __device__ __forceinline__ void seg_pair_load(const SegmentedArgs<T>& a, long lo
     const uint4* p = reinterpret_cast<const uint4*>(a.in + e0);
 #pragma unroll
     for (int q = 0; q < K * (int)sizeof(T) / 16; ++q) {
-      const uint4 u = ld_hint(p + q, pol);
+      const uint4 u = ld_hint_l1(p + q, pol);
       memcpy(&x[q * 16 / sizeof(T)], &u, 16);
     }
     unsigned w[4];  // the lane's K flag bytes (16, or 8 for 8-byte elements)
