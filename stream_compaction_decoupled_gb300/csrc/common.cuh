@@ -271,6 +271,13 @@ __device__ __forceinline__ uint4 ld_hint_l1(const uint4* p, unsigned long long p
                : "l"(p), "l"(pol));
   return r;
 }
+// One 32-byte load (sm_100 and later; p 32-byte aligned) with an L2 policy: a lane
+// that owns 64 consecutive bytes reads them in two instructions of whole sectors.
+__device__ __forceinline__ void ld_hint32(const void* p, unsigned long long pol, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+               : "l"(p), "l"(pol));
+}
 __device__ __forceinline__ void st_hint(uint4* p, uint4 v, unsigned long long pol) {
   asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w), "l"(pol)

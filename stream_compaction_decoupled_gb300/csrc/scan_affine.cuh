@@ -91,10 +91,20 @@ __device__ __forceinline__ void aff_load(Aff<T> (&x)[K], const T* in, long long 
   static_assert(K * sizeof(Aff<T>) == 64, "a lane owns 64 bytes");
   if (vec && e0 + K <= n) {
     const uint4* p = reinterpret_cast<const uint4*>(in + 2 * e0);
+    if (((uintptr_t)p & 31) == 0) {  // two loads of whole sectors
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 u = ld_hint_l1(p + q, pol);
-      memcpy(reinterpret_cast<char*>(x) + 16 * q, &u, 16);
+      for (int q = 0; q < 4; q += 2) {
+        uint4 lo, hi;
+        ld_hint32(p + q, pol, lo, hi);
+        memcpy(reinterpret_cast<char*>(x) + 16 * q, &lo, 16);
+        memcpy(reinterpret_cast<char*>(x) + 16 * q + 16, &hi, 16);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = ld_hint_l1(p + q, pol);
+        memcpy(reinterpret_cast<char*>(x) + 16 * q, &u, 16);
+      }
     }
   } else {
 #pragma unroll

@@ -70,10 +70,21 @@ __device__ __forceinline__ void seg_pair_load(const SegmentedArgs<T>& a, long lo
   const long long e0 = c * CH + (long long)lane * K;
   if (a.vec && c * CH + CH <= a.n) {
     const uint4* p = reinterpret_cast<const uint4*>(a.in + e0);
+    constexpr int Q = K * (int)sizeof(T) / 16;  // 16-byte pieces of the lane's values
+    if (Q % 2 == 0 && ((uintptr_t)p & 31) == 0) {  // loads of whole sectors
 #pragma unroll
-    for (int q = 0; q < K * (int)sizeof(T) / 16; ++q) {
-      const uint4 u = ld_hint_l1(p + q, pol);
-      memcpy(&x[q * 16 / sizeof(T)], &u, 16);
+      for (int q = 0; q < Q; q += 2) {
+        uint4 lo, hi;
+        ld_hint32(p + q, pol, lo, hi);
+        memcpy(&x[q * 16 / sizeof(T)], &lo, 16);
+        memcpy(&x[(q + 1) * 16 / sizeof(T)], &hi, 16);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        const uint4 u = ld_hint_l1(p + q, pol);
+        memcpy(&x[q * 16 / sizeof(T)], &u, 16);
+      }
     }
     unsigned w[4];  // the lane's K flag bytes (16, or 8 for 8-byte elements)
     if constexpr (K == 16) {
