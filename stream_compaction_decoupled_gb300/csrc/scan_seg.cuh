@@ -549,10 +549,20 @@ __device__ __forceinline__ void lane_load(T (&x)[KH], const T* in, long long e0,
   constexpr int VEC = Vec<T>::N;
   if (e0 + KH <= n) {
     const uint4* p = reinterpret_cast<const uint4*>(in + e0);
+    if ((KH / VEC) % 2 == 0 && ((uintptr_t)p & 31) == 0) {  // 32-byte loads of whole sectors
 #pragma unroll
-    for (int j = 0; j < KH / VEC; ++j) {
-      const uint4 u = ld_hint_l1(p + j, pol);
-      memcpy(&x[j * VEC], &u, 16);
+      for (int j = 0; j < KH / VEC; j += 2) {
+        uint4 lo, hi;
+        ld_hint32(p + j, pol, lo, hi);
+        memcpy(&x[j * VEC], &lo, 16);
+        memcpy(&x[(j + 1) * VEC], &hi, 16);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < KH / VEC; ++j) {
+        const uint4 u = ld_hint_l1(p + j, pol);
+        memcpy(&x[j * VEC], &u, 16);
+      }
     }
   } else {
 #pragma unroll
