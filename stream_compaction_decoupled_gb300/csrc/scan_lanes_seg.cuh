@@ -139,7 +139,7 @@ template <class T, int OP, class G>
 __global__ void __launch_bounds__(G::NT, G::MINB)
     scan_lanes_seg_kernel(LanesSegArgs<T, G::C> a, LanesSegStatus<T, G::C> st) {
   pdl_entry();
-  constexpr int NW = G::NW, V = G::V, C = G::C, E = G::E, ROUNDS = G::ROUNDS, CHE = G::CHE, CH = G::CH;
+  constexpr int NW = G::NW, V = G::V, C = G::C, ROUNDS = G::ROUNDS, CH = G::CH;
   __shared__ unsigned s_seg;
   __shared__ T s_w[NW][C];  // warp totals, then their inclusive scan over the warps
   __shared__ T s_base[C];
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB)
   __shared__ int s_phas[GG];
   __shared__ int s_tmo;                  // a gatherer's wait ran out
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slot = lane % V, member = lane / V;
+  const int slot = lane % V;
   if (tid == 0) {
     s_seg = atomicAdd(a.counter, 1u);
     s_tmo = 0;
