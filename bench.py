@@ -79,6 +79,7 @@ KERNEL_SOURCES = {
     "scan_lanes_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "scan_lanes_seg.cuh"),
     "scan_affine_seg_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "scan_affine.cuh"),
     "scan_affine_tile_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_seg.cuh", "scan_affine.cuh"),
+    "scan_strips_kernel": ("common.cuh", "tile.cuh", "launch.h", "scan_strips.cuh"),
 }
 
 

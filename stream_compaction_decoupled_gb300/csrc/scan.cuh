@@ -11,6 +11,7 @@
 #include "scan_lanes.cuh"
 #include "scan_lanes_rts.cuh"
 #include "scan_lanes_seg.cuh"
+#include "scan_strips.cuh"
 #include "scan_rows.cuh"
 #include "scan_seg.cuh"
 #include "scan_stash.cuh"
@@ -26,8 +27,13 @@ template <class T> size_t scan_temp_bytes(long long B, long long R, long long C)
     const size_t m = rows > stash ? rows : stash;
     return m > seg ? m : seg;
   }
-  if (lanes_rts_applies<T>(B, R, C)) return lanes_rts_temp_bytes<T>(B, R, C);
-  const size_t lt = lanes_temp_bytes<T>(B, R, C);
+  const size_t sp = strips_temp_bytes<T>(C);  // the strip kernel may run (it depends on the pointers)
+  if (lanes_rts_applies<T>(B, R, C)) {
+    const size_t rt = lanes_rts_temp_bytes<T>(B, R, C);
+    return rt > sp ? rt : sp;
+  }
+  size_t lt = lanes_temp_bytes<T>(B, R, C);
+  if (sp > lt) lt = sp;
   if constexpr (sizeof(T) == 4) {
     if (B == 1 && (C == 4 || C == 8 || C == 16)) {  // the lane segment kernel may run
       const size_t st = lanes_seg_temp_bytes<T>();
@@ -76,6 +82,14 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
       case OP_MAX: return launch_rows_op<T, OP_MAX>(job, ctx);
       case OP_MUL: return launch_rows_op<T, OP_MUL>(job, ctx);
       default: return launch_rows_op<T, OP_MIN>(job, ctx);
+    }
+  }
+  if (strips_applies<T>(job, ctx.num_sms)) {
+    switch (job.op) {
+      case OP_ADD: return launch_strips_op<T, OP_ADD>(job, ctx);
+      case OP_MAX: return launch_strips_op<T, OP_MAX>(job, ctx);
+      case OP_MUL: return launch_strips_op<T, OP_MUL>(job, ctx);
+      default: return launch_strips_op<T, OP_MIN>(job, ctx);
     }
   }
   if constexpr (sizeof(T) == 4) {
