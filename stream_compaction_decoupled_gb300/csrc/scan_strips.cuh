@@ -18,8 +18,8 @@
 // groups of a warp, then one warp over the warp totals), and each thread rescans its
 // rows seeded with everything before them and stores them.  Rows past R are read as
 // zero: they only reach outputs past R, which are not stored (a scan propagates
-// forward).  Measured on GB300 (fp32 4096 x 4096 down the columns, 256 strips): 32.1
-// us against 40.6 us for the lane kernel; strips of 32 bytes (512 of them, better
+// forward).  Measured on GB300 (fp32 4096 x 4096 down the columns, 256 strips): 30.1-
+// 30.8 us against 40.6 us for the lane kernel; strips of 32 bytes (512 of them, better
 // spread over the SMs) took 49.3 us, each row piece then being a lone DRAM sector.
 #pragma once
 
@@ -91,53 +91,76 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_strips_kernel(StripsArgs<
   const long long chains = a.B * a.strips;
   // This CTA's work: chains blockIdx.x, blockIdx.x + gridDim.x, ..., each a.tiles tiles,
   // taken as one sequence of items so that copies run ahead across chain boundaries.
+  // Two cursors walk it (requests P items ahead of the scan); divisions happen once a
+  // chain, not once a tile.
   const long long my_chains = (chains - blockIdx.x + gridDim.x - 1) / gridDim.x;
   const long long items = my_chains * a.tiles;
+  struct Cursor {
+    long long ch, tl;  // chain, tile in the chain
+    long long c0;      // this thread's first lane
+    long long off;     // element offset of the chain's row 0 at lane c0
+  };
+  auto start_chain = [&](Cursor& k) {
+    const long long b = a.strips == 1 ? k.ch : k.ch / a.strips, sp = k.ch - b * a.strips;
+    k.c0 = sp * W + (long long)q * VEC;
+    k.off = b * a.R * a.C + k.c0;
+  };
+  auto advance = [&](Cursor& k) {
+    if (++k.tl == a.tiles) {
+      k.tl = 0;
+      k.ch += gridDim.x;
+      if (k.ch < chains) start_chain(k);
+    }
+  };
+  Cursor rq{(long long)blockIdx.x, 0, 0, 0}, sc{(long long)blockIdx.x, 0, 0, 0};
+  start_chain(rq);
+  start_chain(sc);
+  int rq_buf = 0, sc_buf = 0;
 
-  // Request item j's rows of this thread into buffer j mod NBUF (zeros past R or C).
-  auto request = [&](long long j) {
-    if (j < items) {
-      const long long ch = blockIdx.x + (j / a.tiles) * gridDim.x, tl = j % a.tiles;
-      const long long b = ch / a.strips, sp = ch - b * a.strips;
-      const long long c0 = sp * W + (long long)q * VEC;
-      const T* src = a.in + b * a.R * a.C + c0;
-      uint4* buf = strips_smem + (size_t)(j % NBUF) * L * NT;
+  // Request the rows of item rq of this thread into buffer rq_buf (zeros past R or C).
+  long long requested = 0;
+  auto request = [&]() {
+    if (requested < items) {
+      const long long r = rq.tl * RT + (long long)g * L;
+      const T* p = a.in + rq.off + r * a.C;
+      uint4* buf = strips_smem + (size_t)rq_buf * L * NT + tid;
+      const bool cv = rq.c0 < a.C;
 #pragma unroll
       for (int i = 0; i < L; ++i) {
-        const long long r = tl * RT + (long long)g * L + i;
-        const bool ok = c0 < a.C && r < a.R;
-        cp_async16(buf + i * NT + tid, ok ? (const void*)(src + r * a.C) : (const void*)a.in, ok ? 16u : 0u);
+        const bool ok = cv && r + i < a.R;
+        cp_async16(buf + i * NT, ok ? (const void*)p : (const void*)a.in, ok ? 16u : 0u);
+        p += a.C;
       }
+      advance(rq);
+      rq_buf = rq_buf + 1 == NBUF ? 0 : rq_buf + 1;
+      ++requested;
     }
     cp_async_commit();  // an empty group past the end keeps the group count in step
   };
 #pragma unroll
-  for (int k = 0; k < P; ++k) request(k);
+  for (int k = 0; k < P; ++k) request();
 
   const unsigned long long drop = l2_policy_evict_first();
   Vec<T> carry;  // everything before the current tile in this thread's lanes
   bool hc = false;
   for (long long j = 0; j < items; ++j) {
-    request(j + P);
+    request();
     cp_async_wait<P>();  // item j has landed (this thread's own rows only: no barrier)
-    const long long ch = blockIdx.x + (j / a.tiles) * gridDim.x, tl = j % a.tiles;
-    const long long b = ch / a.strips, sp = ch - b * a.strips;
-    const long long c0 = sp * W + (long long)q * VEC;
-    const bool qvalid = c0 < a.C;  // C is a multiple of VEC
-    const long long r0 = tl * RT;
-    if (tl == 0) {  // a new chain
+    const bool qvalid = sc.c0 < a.C;  // C is a multiple of VEC
+    const long long r0 = sc.tl * RT;
+    if (sc.tl == 0) {  // a new chain
       hc = false;
       if (!a.inclusive) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) carry.v[e] = qvalid ? a.init[(c0 + e) % a.init_lanes] : T{};
+        for (int e = 0; e < VEC; ++e) carry.v[e] = qvalid ? a.init[(sc.c0 + e) % a.init_lanes] : T{};
         hc = true;
       }
     }
-    const uint4* buf = strips_smem + (size_t)(j % NBUF) * L * NT;
+    const uint4* buf = strips_smem + (size_t)sc_buf * L * NT + tid;
     Vec<T> x[L];
 #pragma unroll
     for (int i = 0; i < L; ++i) {
-      const uint4 u = buf[i * NT + tid];
+      const uint4 u = buf[i * NT];
       memcpy(x[i].v, &u, 16);
     }
 
@@ -177,7 +200,7 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_strips_kernel(StripsArgs<
       hb = true;
     }
     const Vec<T> tile_total = s_wt[NW - 1][q];
-    T* dst = a.out + b * a.R * a.C + c0;
+    T* dst = a.out + sc.off + (r0 + (long long)g * L) * a.C;
 #pragma unroll
     for (int i = 0; i < L; ++i) {
       const long long r = r0 + (long long)g * L + i;
@@ -193,11 +216,14 @@ __global__ void __launch_bounds__(G::NT, G::MINB) scan_strips_kernel(StripsArgs<
       if (qvalid && r < a.R) {
         uint4 u;
         memcpy(&u, y.v, 16);
-        st_hint(reinterpret_cast<uint4*>(dst + r * a.C), u, drop);
+        st_hint(reinterpret_cast<uint4*>(dst), u, drop);
       }
+      dst += a.C;
     }
     carry = hc ? vec_then<T, OP>(carry, tile_total) : tile_total;
     hc = true;
+    advance(sc);
+    sc_buf = sc_buf + 1 == NBUF ? 0 : sc_buf + 1;
     __syncthreads();  // s_wt is rewritten by the next tile
   }
   cp_async_wait<0>();
