@@ -106,3 +106,20 @@ def test_strips_call_status_is_clean():
     temp.fill_(0xFF)  # a stale status word from some earlier use
     gb.scan_batched(x, axis=0, temp=temp)
     assert gb.last_device_error(temp) == gb.OK
+
+
+@pytest.mark.parametrize("dt,rows,cols,lanes", [("f32", 12, 300, 256), ("i32", 10, 513, 272), ("i64", 12, 700, 128),
+                                                ("f32", 3, 1025, 1024)])
+def test_strips_rows_of_lane_vectors(dt, rows, cols, lanes):
+    """Rows of lane-vector elements scanned along the rows: every row is its own set of
+    chains (B > 1), with enough strips in all to take the strip kernel."""
+    x = values(dt, "add", rows * cols * lanes, rows + cols + lanes, lanes)
+    xd = dev(x).reshape(rows, cols, lanes)
+    got = gb.scan_batched(xd, axis=1, lanes=lanes).cpu().numpy()
+    assert_scan_matches(got, as3(x, rows, cols, lanes), "add", True, what="rows of %d lanes" % lanes)
+    init = (np.arange(lanes) % 13).astype(NP[dt])
+    got = gb.scan_batched(xd, axis=1, lanes=lanes, inclusive=False, init=init).cpu().numpy()
+    assert_scan_matches(got, as3(x, rows, cols, lanes), "add", False, init, what="rows excl %d lanes" % lanes)
+    got = gb.scan_batched(xd, axis=1, op="max", lanes=lanes).cpu().numpy()
+    assert_scan_matches(got, as3(x, rows, cols, lanes), "max", True, what="rows max %d lanes" % lanes)
+    assert gb.device_error() == gb.OK
