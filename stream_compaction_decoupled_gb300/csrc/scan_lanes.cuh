@@ -50,10 +50,12 @@ template <class T, int RPG_ = 32, int D_ = 4, int CTMAX_ = 0> struct LanesGeomT 
   // lane workload measured (96-byte structs 1e6: 51.9 / 59.5 / 62.1 us at 4 / 8 / 16;
   // 17-lane duals 1e6: 162 / 176 / 232 us): wider windows cost registers and occupancy.
   static constexpr int D = D_;
-  // Strip width: 256-byte strips.  Wider strips (fewer, larger per-row copies, longer
-  // chains) measured slower everywhere (4096 x 4096 fp32 columns: 43.6 / 49.8 / 62.0 us
-  // at 64 / 128 / 256 lanes; 1000 x 1e4 fp64: 72-74 / 74.3 / 76.4 us at 32 / 64 / 128).
-  static constexpr int CTMAX = CTMAX_ > 0 ? CTMAX_ : (sizeof(T) == 4 ? 64 : 32);
+  // Strip width: 128-byte strips for 4-byte lanes, 256-byte for 8-byte.  Wider strips
+  // (fewer, larger per-row copies, longer chains) measured slower everywhere (4096 x
+  // 4096 fp32 columns: 43.6 / 49.8 / 62.0 us at 64 / 128 / 256 lanes; 1000 x 1e4 fp64:
+  // 72-74 / 74.3 / 76.4 us at 32 / 64 / 128), and 32 fp32 lanes beat 64 on 2080-byte
+  // elements (32.9 against 35.0 us: twice the chains, half as long).
+  static constexpr int CTMAX = CTMAX_ > 0 ? CTMAX_ : 32;
   static int ct(long long C) { return C <= CTMAX ? (int)C : CTMAX; }
   static int groups(int CT) {
     int g = NT / CT;
