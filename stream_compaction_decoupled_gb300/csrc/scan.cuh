@@ -51,10 +51,10 @@ template <class T> cudaError_t launch_scan(const ScanJob& job, const LaunchCtx& 
   if constexpr (std::is_same<T, double>::value) {
     if (seg_chunk_applies<T>(job, ctx.num_sms)) {
       switch (job.op) {
-        case OP_ADD: return launch_seg_chunk_op<T, OP_ADD>(job, ctx);
-        case OP_MAX: return launch_seg_chunk_op<T, OP_MAX>(job, ctx);
-        case OP_MUL: return launch_seg_chunk_op<T, OP_MUL>(job, ctx);
-        default: return launch_seg_chunk_op<T, OP_MIN>(job, ctx);
+        case OP_ADD: return launch_seg_chunk<T, OP_ADD>(job, ctx);
+        case OP_MAX: return launch_seg_chunk<T, OP_MAX>(job, ctx);
+        case OP_MUL: return launch_seg_chunk<T, OP_MUL>(job, ctx);
+        default: return launch_seg_chunk<T, OP_MIN>(job, ctx);
       }
     }
   }

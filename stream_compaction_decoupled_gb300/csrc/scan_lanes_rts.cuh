@@ -210,61 +210,61 @@ __global__ void __launch_bounds__(Gm::NT, 3) lanes_rts_reduce_kernel(LanesRtsArg
   }
 }
 
-// One CTA per chain: exclusive range prefixes per lane, in place.  Thread (c, j) holds
-// the j-th of J contiguous parts of the chain's K ranges (at most U of them) in
-// registers: it folds them, the part totals are scanned per lane (Hillis-Steele over
-// j in shared memory, log2 J steps), and it writes the running prefixes back.  Range
-// 0's entry is left as it is (it has no prefix).
+// One CTA per lane of each chain: the exclusive range prefixes of that lane, in place.
+// Thread j holds the j-th of J = min(K, 1024) contiguous parts of the K ranges (at most
+// U of them) in registers and folds them; the part totals are scanned by warp shuffles
+// and one warp over the warp totals; each thread writes its running prefixes back.
+// Range 0's entry is left as it is (it has no prefix).  Spreading the lanes over CTAs
+// keeps the fp64 adds of a long chain off a single SM (one SM adds about 1.7 doubles a
+// clock: 417 ranges x 17 lanes took 10-12 us on one CTA).
 template <class T, int OP>
 __global__ void __launch_bounds__(1024) lanes_rts_spine_kernel(LanesRtsArgs<T> a) {
   pdl_entry();
   constexpr int U = lanes_spine_u<T>();
-  __shared__ T s_part[2][1024];
-  const int tid = threadIdx.x, CT = a.CT;
-  const unsigned K = a.K;
-  int J = 1024 / CT;
-  if ((unsigned)J > K) J = (int)K;
-  const int c = tid % CT, j = tid / CT;
-  const unsigned strip = blockIdx.x % a.strips;
-  const long long cols_left = a.C - (long long)strip * CT;
-  const int cols = cols_left >= CT ? CT : (int)cols_left;
-  T* chain = a.agg + (size_t)blockIdx.x * K * CT;
-  const bool part = j < J && c < cols;
-  const unsigned pb = part ? (unsigned)((unsigned long long)j * K / J) : 0u;
-  const unsigned pe = part ? (unsigned)((unsigned long long)(j + 1) * K / J) : 0u;  // 0 < pe - pb <= U
-  T* mine = chain + (size_t)pb * CT + c;
+  __shared__ T s_w[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, CT = a.CT;
+  const unsigned K = a.K, chain = blockIdx.x / CT;
+  const int c = (int)(blockIdx.x - chain * CT);
+  const unsigned strip = chain % a.strips;
+  if ((long long)strip * CT + c >= a.C) return;  // a lane past C (the CTA leaves as one)
+  const unsigned J = K < 1024u ? K : 1024u;
+  const bool part = (unsigned)tid < J;  // the parts are threads 0 .. J-1: later threads never reach them
+  const unsigned pb = part ? (unsigned)((unsigned long long)tid * K / J) : 0u;
+  const unsigned pe = part ? (unsigned)((unsigned long long)(tid + 1) * K / J) : 0u;  // 0 < pe - pb <= U
+  T* mine = a.agg + ((size_t)chain * K + pb) * CT + c;
   const int cnt = (int)(pe - pb);
-  T v[U];
+  T v[U] = {};
 #pragma unroll
   for (int q = 0; q < U; ++q)
-    if (q < cnt) v[q] = mine[q * CT];
-  if (part) {
-    T acc = v[0];
+    if (q < cnt) v[q] = mine[(size_t)q * CT];
+  T acc = v[0];  // unused past J: scans only pull from lower threads
 #pragma unroll
-    for (int q = 1; q < U; ++q)
-      if (q < cnt) acc = Op<T, OP>::f(acc, v[q]);
-    s_part[0][j * CT + c] = acc;
-  }
+  for (int q = 1; q < U; ++q)
+    if (q < cnt) acc = Op<T, OP>::f(acc, v[q]);
+  const T inc = warp_inclusive<T, OP>(acc, lane);
+  if (lane == 31) s_w[warp] = inc;
   __syncthreads();
-  int in = 0;
-  for (int d = 1; d < J; d <<= 1) {  // inclusive scan of the part totals, per lane
-    if (part) {
-      T x = s_part[in][j * CT + c];
-      if (j >= d) x = Op<T, OP>::f(s_part[in][(j - d) * CT + c], x);
-      s_part[in ^ 1][j * CT + c] = x;
-    }
-    __syncthreads();
-    in ^= 1;
-  }
-  if (part) {
-    bool has = j > 0;
-    T run = has ? s_part[in][(j - 1) * CT + c] : T{};
+  if (warp == 0) s_w[lane] = warp_inclusive<T, OP>(s_w[lane], lane);
+  __syncthreads();
+  const T below = __shfl_up_sync(0xffffffffu, inc, 1);  // the parts before this one in the warp
+  if (part && tid > 0) {
+    T run;
+    if (warp == 0) run = below;
+    else run = lane == 0 ? s_w[warp - 1] : Op<T, OP>::f(s_w[warp - 1], below);
 #pragma unroll
     for (int q = 0; q < U; ++q) {
       if (q < cnt) {
-        if (has) mine[q * CT] = run;  // the prefix of range pb + q
-        run = has ? Op<T, OP>::f(run, v[q]) : v[q];
-        has = true;
+        mine[(size_t)q * CT] = run;  // the prefix of range pb + q
+        run = Op<T, OP>::f(run, v[q]);
+      }
+    }
+  } else if (part) {  // thread 0: range 0 keeps its aggregate, the rest of its part gets prefixes
+    T run = v[0];
+#pragma unroll
+    for (int q = 1; q < U; ++q) {
+      if (q < cnt) {
+        mine[(size_t)q * CT] = run;
+        run = Op<T, OP>::f(run, v[q]);
       }
     }
   }
@@ -524,7 +524,7 @@ cudaError_t launch_lanes_rts_op(const ScanJob& job, const LaunchCtx& ctx) {
     e = cudaMemcpyAsync(init_area, job.init_host, (size_t)job.init_lanes * sizeof(T), cudaMemcpyHostToDevice,
                         ctx.stream);
   if (e == cudaSuccess) e = launch_pdl(lanes_rts_reduce_kernel<T, OP, Gm>, ranges, Gm::NT, 0, ctx.stream, a);
-  if (e == cudaSuccess) e = launch_pdl(lanes_rts_spine_kernel<T, OP>, p.chains, 1024, 0, ctx.stream, a);
+  if (e == cudaSuccess) e = launch_pdl(lanes_rts_spine_kernel<T, OP>, p.chains * p.t.CT, 1024, 0, ctx.stream, a);
   if (e == cudaSuccess) e = launch_pdl(lanes_rts_scan_kernel<T, OP, Gm>, ranges, Gm::NT, 0, ctx.stream, a);
   profile_after(ctx);
   return e;

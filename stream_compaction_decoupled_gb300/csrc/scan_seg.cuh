@@ -538,11 +538,14 @@ template <class T, int NT_, int KH_, int NH_, int MAXCPW_, int MINB_> struct Seg
   static_assert(KH % VEC == 0, "whole vectors per lane");
   static_assert(sizeof(T) != 8 || KH == 16, "the staging swizzle is laid out for 16 doubles a lane");
 };
-// 512 threads (128 registers a thread), 16 doubles a lane, up to 12 chunks a warp
-// (112 KB of shared memory).  Measured on GB300, fp64 add, L2 flushed: 21.2 / 68.3 /
-// 82.6 us at 1e6 / 1e7 / 1.26e7 elements against 31.2 / 115.3 / 133.8 us for the row
-// kernel's chunked variant.
-template <class T> using SegChunkGeom = SegChunkCfg<T, 512, 16, 1, 12, 1>;
+// 512 threads (126 registers a thread), 16 doubles a lane in registers at once, up to 12
+// chunks a warp (112 KB of shared memory).  A lane owns 32 or 48 consecutive doubles of
+// a chunk (two or three register loads): the warp scan and base of each chunk (7 adds a
+// lane) are then spread over more elements, 2.22 or 2.15 adds per element against 2.44
+// for 16.  Measured on GB300, fp64 add, L2 flushed, 1e7 elements: 65.4-65.9 us for 16
+// doubles a lane, 61.8-62.0 us for 32, 59.7-59.8 us for 48, 63.9-65.3 us for 64.
+template <class T> using SegChunkGeom = SegChunkCfg<T, 512, 16, 2, 12, 1>;
+template <class T> using SegChunkGeomL = SegChunkCfg<T, 512, 16, 3, 12, 1>;
 
 template <class T, int KH>
 __device__ __forceinline__ void lane_load(T (&x)[KH], const T* in, long long e0, long long n, unsigned long long pol) {
@@ -738,14 +741,27 @@ template <class G> bool seg_chunk_plan_fits(const SegPlan& p) {
   return p.ctas > 0 && p.cpw <= G::MAXCPW;
 }
 
-template <class T, class G = SegChunkGeom<T>> bool seg_chunk_applies(const ScanJob& job, int num_sms) {
+// Of the two lane lengths, the one whose busiest warp holds fewer elements (its chunk
+// count times the chunk), the shorter on a tie: measured at 1e6 / 3e6 / 1e7 / 1.2e7
+// doubles (19.1 / 29.3 / 61.9 / 70.3 us with 32 a lane, 19.1 / 27.2 / 59.7 / 72.3 us
+// with 48), this picks the faster each time.
+template <class T> bool seg_chunk_long(long long n, int num_sms) {
+  using G2 = SegChunkGeom<T>;
+  using G3 = SegChunkGeomL<T>;
+  const SegPlan p2 = seg_plan<G2>(1, n, num_sms), p3 = seg_plan<G3>(1, n, num_sms);
+  return p3.cpw * G3::CH < p2.cpw * G2::CH;
+}
+
+template <class T> bool seg_chunk_applies(const ScanJob& job, int num_sms) {
   if (!(job.B == 1 && job.C == 1 && (uintptr_t)job.in % 16 == 0 && (uintptr_t)job.out % 16 == 0 &&
         job.R * (long long)sizeof(T) <= kSegMaxBytes))
     return false;
-  return seg_chunk_plan_fits<G>(seg_plan<G>(1, job.R, num_sms));
+  if (seg_chunk_long<T>(job.R, num_sms))
+    return seg_chunk_plan_fits<SegChunkGeomL<T>>(seg_plan<SegChunkGeomL<T>>(1, job.R, num_sms));
+  return seg_chunk_plan_fits<SegChunkGeom<T>>(seg_plan<SegChunkGeom<T>>(1, job.R, num_sms));
 }
 
-template <class T, int OP, class G = SegChunkGeom<T>>
+template <class T, int OP, class G>
 cudaError_t launch_seg_chunk_op(const ScanJob& job, const LaunchCtx& ctx) {
   const SegPlan p = seg_plan<G>(1, job.R, ctx.num_sms);
   if (p.ctas == 0 || !seg_chunk_plan_fits<G>(p)) return cudaErrorInvalidValue;  // callers check seg_chunk_applies
@@ -774,6 +790,11 @@ cudaError_t launch_seg_chunk_op(const ScanJob& job, const LaunchCtx& ctx) {
   if (e == cudaSuccess) e = launch_pdl(kern, p.ctas, G::NT, G::SMEM, ctx.stream, a, st);
   profile_after(ctx);
   return e;
+}
+
+template <class T, int OP> cudaError_t launch_seg_chunk(const ScanJob& job, const LaunchCtx& ctx) {
+  return seg_chunk_long<T>(job.R, ctx.num_sms) ? launch_seg_chunk_op<T, OP, SegChunkGeomL<T>>(job, ctx)
+                                               : launch_seg_chunk_op<T, OP, SegChunkGeom<T>>(job, ctx);
 }
 
 }  // namespace gbs
